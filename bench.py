@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the deterministic shape-adaptive GEMM on GB300.
+
+One step = one GEMM C = alpha*A*B + beta*C through the C ABI on one batch
+of seeded synthetic inputs (the whole hot path). The default workload is
+the TF32 2048^3 GEMM with N(0,1) inputs (alpha 1, beta 0, seed 1); the
+metric is TFLOP/s = 2*M*N*K / t.
+
+Timing: W untimed warm-up steps, then exactly K timed steps between a
+barrier + device synchronisation on both sides. Each step writes a 256 MiB
+buffer first (outside its timing) so that L2 (129 MB) holds none of the
+operands, then records a CUDA event pair on the launching stream around the
+gemm_run call. ``value`` = steps x FLOP / sum of step times (max over
+ranks, x ranks for the whole job). ``e2e`` runs the same GEMM through
+gemm_run_host from pinned host buffers, copies included.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference      # the FP64 CPU oracle on host cores
+  python bench.py --all results.json    # every workload, one line each (not the driver line)
+Under torchrun every rank runs its own replica (the GEMM has no exchange
+step); the line reports the whole job.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth_inputs as si  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2MNK/t) per dtype/shape; % of GB300 dense tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT = "tf32-square2048"
+NOMINAL_TFLOPS = {"bf16": 2250.0, "fp16": 2250.0, "tf32": 1100.0}
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20
+
+
+def workloads():
+    return {f"{w[1]}-{w[0]}": w for w in si.WORKLOADS}
+
+
+def describe_workload(w):
+    name, dt, (M, N, K), fam, alpha, beta, cfam, seed, _ = w
+    dist = {"normal": "N(0,1)", "uniform": "U(-1,1)", "dyadic": "integers in [-4,4]"}[fam]
+    c = f", C0 {dist if cfam == fam else 'N(0,1)'}" if cfam else ""
+    return f"{dt} GEMM M={M} N={N} K={K}, A,B {dist}, alpha={alpha:g}, beta={beta:g}{c}, seed {seed}"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def tensor_peak(dtype, pk):
+    """Dense peak for the contraction's own dtype: the measured bf16 burst
+    figure times the nominal dtype ratio."""
+    return pk["bf16_tflops"] * NOMINAL_TFLOPS[dtype] / NOMINAL_TFLOPS["bf16"]
+
+
+def min_bytes(dtype, M, N, K, beta):
+    es = 4 if dtype == "tf32" else 2
+    return es * (M * K + K * N) + 4 * M * N * (2 if beta != 0 else 1)
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.rows = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, start):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if self.t_start and self.t_start <= t <= (self.t_stop or t)]
+        use = inside or [r for _, r in self.rows]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO("\n".join(use))):
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+                for n, v in zip(names, row[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": len(inside)}
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_sample(w, budget_s):
+    """Time the FP64 oracle (as it stands) on whole repeats of the workload,
+    or on a leading block of rows when one full problem would exceed the
+    budget. Returns (TFLOP/s, threads, description, seconds)."""
+    import oracle
+    name, dt, (M, N, K), fam, alpha, beta, cfam, seed, _ = w
+    A, B, C0 = si.problem(M, N, K, dt, fam, seed, cfam)
+    oracle.build()
+    # probe on a few rows to size the sample
+    probe_rows = max(1, min(M, 16))
+    t0 = time.perf_counter()
+    oracle.gemm(A, B, C0, alpha, beta, dt, 0, probe_rows)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    rows = M
+    repeats = max(1, int(budget_s / max(per_row * M, 1e-9)))
+    if per_row * M > budget_s:
+        rows = max(1, int(budget_s / per_row))
+        repeats = 1
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.gemm(A, B, C0, alpha, beta, dt, 0, rows)
+    dt_s = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K * repeats
+    what = (f"{repeats} full {M}x{N}x{K} problem(s)" if rows == M
+            else f"rows 0..{rows - 1} of the {M}x{N}x{K} problem ({rows * N} of {M * N} outputs)")
+    return flops / dt_s / 1e12, oracle.threads(), what, dt_s
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    steps = []
+    per_step_budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        tflops, cores, what, secs = oracle_sample(w, per_step_budget)
+        if i >= args.warmup:
+            steps.append((tflops, secs))
+    total_s = sum(s for _, s in steps)
+    flops_total = sum(t * s * 1e12 for t, s in steps)
+    value = flops_total / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / max(1, len(steps)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe_workload(w), "name": args.workload},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {what}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def traffic_for(desc):
+    """DRAM bytes per launch recorded from an ncu capture of this exact
+    kernel source, or None (no capture, or the source changed since)."""
+    from shape_adaptive_tile_gb300.build import source_hash
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    key = desc.split(":")[0].strip()
+    cur = source_hash()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or "|" not in line:
+                continue
+            parts = [p.strip() for p in line.split("|")]
+            if len(parts) >= 3 and parts[0] == key and parts[1] == cur:
+                return int(float(parts[2]))
+    return None
+
+
+def bench_one(args, w, rank, world, torch, sat, quiet=False):
+    name, dt, (M, N, K), fam, alpha, beta, cfam, seed, _ = w
+    A, B, C0 = si.problem(M, N, K, dt, fam, seed, cfam)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def to_dev(x, bf=False):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+    dA, dB = to_dev(A, dt == "bf16"), to_dev(B, dt == "bf16")
+    dC = to_dev(C0) if C0 is not None else torch.zeros(M, N, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    plan = sat.Plan(M, N, K, dt)
+    desc = plan.describe()
+    flops = 2.0 * M * N * K
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan.run(dA, dB, dC, alpha, beta, sptr)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device()) if not quiet else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(True)
+    launches = 0
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        plan.run(dA, dB, dC, alpha, beta, sptr)
+        e1.record(stream)
+        launches += 1
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if clocks:
+        clocks.mark(False)
+        time.sleep(0.2)
+        clocks.stop()
+    times = [e0.elapsed_time(e1) for e0, e1 in ev]
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    sat.check(plan.status())
+    res = {"plan": desc, "flops": flops, "times_ms": times, "total_ms": total_ms, "launches": launches,
+           "clocks": clocks.summary() if clocks else None, "dtype": dt, "M": M, "N": N, "K": K,
+           "alpha": alpha, "beta": beta}
+    if quiet:
+        plan.close()
+        return res
+
+    # end to end through gemm_run_host: pinned host operands, copies timed
+    hA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+    hB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+    hC = (torch.from_numpy(C0.copy()) if C0 is not None else torch.zeros(M, N)).pin_memory()
+    eA = torch.empty(hA.shape, dtype=hA.dtype, device=dev)
+    eB = torch.empty(hB.shape, dtype=hB.dtype, device=dev)
+    eC = torch.empty(M, N, device=dev)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, alpha, beta, eA, eB, eC, sptr))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, alpha, beta, eA, eB, eC, sptr))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    es = 4 if dt == "tf32" else 2
+    res["e2e"] = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                  "h2d_bytes_per_step": es * (M * K + K * N) + (4 * M * N if beta != 0 else 0),
+                  "d2h_bytes_per_step": 4 * M * N, "ms_per_step": e2e_ms}
+    plan.close()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(workloads()))
+    ap.add_argument("--all", metavar="JSON", help="bench every workload and write per-workload results")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workloads()[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    import shape_adaptive_tile_gb300 as sat
+    from shape_adaptive_tile_gb300.build import LIB
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 and not os.path.exists(LIB):
+        sat.build()
+    if world > 1:
+        torch.distributed.barrier()
+    sat.lib()
+
+    if args.all:
+        out = []
+        for key in sorted(workloads()):
+            r = bench_one(args, workloads()[key], rank, world, torch, sat, quiet=True)
+            t = sorted(r["times_ms"])
+            med = statistics.median(t)
+            pk, _ = peaks()
+            bound = "tensor"
+            ai = r["flops"] / min_bytes(r["dtype"], r["M"], r["N"], r["K"], r["beta"])
+            if ai < tensor_peak(r["dtype"], pk) * 1e12 / (pk["hbm_gbs"] * 1e9):
+                bound = "hbm"
+            item = {"workload": key, "plan": r["plan"], "median_ms": med, "min_ms": t[0],
+                    "p90_ms": t[int(0.9 * (len(t) - 1))], "samples": len(t),
+                    "tflops_median": r["flops"] / (med * 1e-3) / 1e12, "bound": bound,
+                    "pct_tensor_peak": 100 * r["flops"] / (med * 1e-3) / 1e12 / tensor_peak(r["dtype"], pk),
+                    "pct_hbm": 100 * min_bytes(r["dtype"], r["M"], r["N"], r["K"], r["beta"]) / (med * 1e-3)
+                    / (pk["hbm_gbs"] * 1e9)}
+            out.append(item)
+            if rank == 0:
+                print(json.dumps(item), flush=True)
+        if rank == 0:
+            with open(args.all, "w") as f:
+                json.dump(out, f, indent=1)
+        return 0
+
+    r = bench_one(args, w, rank, world, torch, sat)
+    pk, pk_src = peaks()
+    ms = r["total_ms"] / args.steps
+    value = world * r["flops"] / (ms * 1e-3) / 1e12
+    peak = tensor_peak(r["dtype"], pk)
+    achieved = r["flops"] / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
+        "config": {"workload": describe_workload(w), "name": args.workload, "M": r["M"], "N": r["N"],
+                   "K": r["K"], "plan": r["plan"], "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "median_ms": statistics.median(r["times_ms"]), "min_ms": min(r["times_ms"])},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic_for(r["plan"]),
+                     "peak_source": f"{pk_src}: bf16 burst {pk['bf16_tflops']} TFLOP/s x "
+                                    f"{NOMINAL_TFLOPS[r['dtype']]}/{NOMINAL_TFLOPS['bf16']} nominal ratio"},
+        "e2e": {k: v for k, v in r["e2e"].items() if k != "ms_per_step"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops, cores, what, secs = oracle_sample(w, 12.0)
+        line["cpu_baseline"] = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{what}, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,146 @@
+/*
+ * Deterministic, shape-adaptive dense GEMM for GB300 (sm_103a): the C ABI.
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * A is M x K, B is K x N, C is M x N, all dense row-major with no padding
+ * (lda = K, ldb = N, ldc = N) and no transposes. A and B are fp32 (computed
+ * on the TF32 tensor cores), bf16 or fp16; accumulation and C are fp32.
+ *
+ * The operation is the GEMM that "Scale coverage exposes a remaining GEMM
+ * gap" measures (section "Measurement contract and evidence": C = A*B,
+ * alpha = 1, beta = 0, compact row-major, no transpose) in its BLAS form
+ * with alpha and beta. "Measured data point on fixed-tile vs shape-adaptive
+ * GEMM" (section "The wall, and why we think it's structural") argues that
+ * what such a library must provide is a per-shape choice of tile and
+ * schedule, not one kernel; gemm_plan_create makes that choice once per
+ * (M, N, K, dtype), and gemm_run executes it. Its section "The actual
+ * question" names the constraint kept here: results are bit-identical from
+ * run to run (no split-K with atomics, a fixed K order per output tile).
+ *
+ * All device pointers are plain CUDA device addresses (for example
+ * torch.Tensor.data_ptr()); the library never allocates, frees or keeps
+ * them. Functions return 0 on success or a negative gemm_status_t; the
+ * message of the last failure on the calling thread is in gemm_last_error().
+ */
+#ifndef SAT_GEMM_H
+#define SAT_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of A and B. C is always fp32. */
+typedef enum {
+    GEMM_TF32 = 0, /* fp32 storage, TF32 tensor-core multiply, fp32 accumulate */
+    GEMM_BF16 = 1, /* bfloat16 storage, fp32 accumulate */
+    GEMM_FP16 = 2  /* IEEE binary16 storage, fp32 accumulate */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_ARG = -1,     /* NULL plan/pointer, negative or oversized dimension, bad dtype */
+    GEMM_ERR_ARCH = -2,    /* current device is not compute capability 10.3 (sm_103) */
+    GEMM_ERR_ALIGN = -3,   /* A/B not aligned to their element size, or C not 4-byte aligned */
+    GEMM_ERR_LAUNCH = -4,  /* a CUDA call failed (message in gemm_last_error) */
+    GEMM_ERR_TIMEOUT = -5, /* a bounded wait inside a kernel gave up (see gemm_plan_status) */
+    GEMM_ERR_NOMEM = -6    /* host or device allocation failed while creating a plan */
+} gemm_status_t;
+
+typedef struct gemm_plan gemm_plan; /* opaque */
+
+/*
+ * Choose the kernel (tile shape, CTA-pair or single SM, stage count, raster
+ * order, load path) for this problem on the CURRENT device, and prepare it.
+ * M, N, K >= 0 and each < 2^31. Allocates host state and one 4-byte device
+ * error word, both owned by the plan. Returns NULL on failure; the reason is
+ * in gemm_last_error(). Must not be called during CUDA stream capture.
+ */
+gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype);
+
+/*
+ * As gemm_plan_create, but with the dispatcher's choice replaced by
+ * `config` = "bn,cg,raster,group" (bn in {64,128,256}; cg 1 or 2, where 2
+ * needs bn >= 128; raster 0 = groups along M, 1 = along N; group >= 1),
+ * optionally followed by ",plain" to force the plain-load producer. NULL or
+ * "" means the dispatcher decides. For sweeps and tests; the result is the
+ * same GEMM whatever the configuration.
+ */
+gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config);
+
+/*
+ * Enqueue C = alpha * A * B + beta * C on `cuda_stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and return without synchronising.
+ *   A: device pointer, M x K elements of the plan's dtype, row-major.
+ *   B: device pointer, K x N elements, row-major.
+ *   C: device pointer, M x N floats, row-major; read only if beta != 0
+ *      (so with beta == 0 any contents, NaN included, are ignored).
+ * M == 0 or N == 0: nothing is done. K == 0 or alpha == 0: C = beta * C.
+ * A and B must be aligned to their element size, C to 4 bytes
+ * (GEMM_ERR_ALIGN otherwise); 16-byte aligned A/B with 16-byte-multiple row
+ * strides take the TMA load path, anything else the plain-load path, with
+ * identical results. The plan is read-only here, so one plan may run on
+ * several streams or threads at once. Launch failures return
+ * GEMM_ERR_LAUNCH; kernel-side bounded-wait timeouts are reported by
+ * gemm_plan_status().
+ */
+int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, float alpha, float beta,
+             void* cuda_stream);
+
+/*
+ * End-to-end form of gemm_run for operands in HOST memory (pinned host
+ * memory gives asynchronous copies): on `cuda_stream`, copy hA -> dA,
+ * hB -> dB and (only if beta != 0) hC -> dC, run the GEMM on the device
+ * buffers, then copy dC -> hC. dA, dB, dC are caller-owned device buffers
+ * of the full operand sizes. Returns after enqueueing; synchronise the
+ * stream before reading hC.
+ */
+int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* hC, float alpha, float beta,
+                  void* dA, void* dB, float* dC, void* cuda_stream);
+
+/* Free the plan and its device error word. NULL is accepted. Synchronises
+ * nothing: do not destroy a plan whose runs may still be executing. */
+void gemm_plan_destroy(gemm_plan* plan);
+
+/*
+ * Synchronise the device, read and clear the plan's device error word.
+ * Returns 0 if no kernel of this plan gave up a bounded wait since the last
+ * call, GEMM_ERR_TIMEOUT if one did, GEMM_ERR_LAUNCH if the device reported
+ * an error.
+ */
+int gemm_plan_status(const gemm_plan* plan);
+
+/* Human-readable description of the chosen configuration, valid for the
+ * plan's lifetime, e.g. "tf32 m2048 n2048 k2048: bn256 cg1 st4 tma raster0 g8 grid128". */
+const char* gemm_plan_describe(const gemm_plan* plan);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* gemm_last_error(void);
+
+/*
+ * Self-test of the kernels' bounded waits: launch one CTA that waits on a
+ * shared-memory barrier nobody arrives at, with a limit of `timeout_ns`
+ * (capped at 1 s), then read the error word. Returns GEMM_ERR_TIMEOUT when
+ * the wait gave up as designed and the context is still usable, another
+ * negative status otherwise. Blocks until the kernel has finished.
+ */
+int gemm_selftest_bounded_wait(uint64_t timeout_ns);
+
+/*
+ * Host-only view of the dispatcher (no device is touched): the choice that
+ * gemm_plan_create would make for this problem on a device with `sm_count`
+ * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
+ * strides are multiples of 16 bytes). Writes "bn,cg,raster,group,source"
+ * (source: rule or table) into `out` (NUL-terminated, at most `out_len`
+ * bytes). Returns 0, or GEMM_ERR_ARG on bad arguments.
+ */
+int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int sm_count, int tma_ok, char* out,
+                       int out_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAT_GEMM_H */

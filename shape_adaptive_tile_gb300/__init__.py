@@ -1,0 +1,168 @@
+"""Deterministic, shape-adaptive dense GEMM for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``include/gemm.h``: the functions
+below have the C names and only marshal arguments; every step of the GEMM
+runs in the library's CUDA kernels. Operand pointers are plain integers
+(for example ``torch.Tensor.data_ptr()``); streams are ``cudaStream_t``
+values (for example ``torch.cuda.current_stream().cuda_stream``).
+
+Nothing here falls back to another implementation: if the library is not
+built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB, build  # noqa: F401  (build is part of the public surface)
+
+GEMM_TF32, GEMM_BF16, GEMM_FP16 = 0, 1, 2
+DTYPES = {"tf32": GEMM_TF32, "bf16": GEMM_BF16, "fp16": GEMM_FP16}
+STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_ARG", -2: "GEMM_ERR_ARCH", -3: "GEMM_ERR_ALIGN",
+          -4: "GEMM_ERR_LAUNCH", -5: "GEMM_ERR_TIMEOUT", -6: "GEMM_ERR_NOMEM"}
+
+# Every function the C ABI exports (include/gemm.h).
+EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_run", "gemm_run_host",
+           "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
+           "gemm_selftest_bounded_wait", "gemm_select_config")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"CUDA library not built ({LIB}); run shape_adaptive_tile_gb300.build()")
+            L = ctypes.CDLL(LIB)
+            i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+            L.gemm_plan_create.argtypes = [i64, i64, i64, i32]
+            L.gemm_plan_create.restype = vp
+            L.gemm_plan_create_config.argtypes = [i64, i64, i64, i32, ctypes.c_char_p]
+            L.gemm_plan_create_config.restype = vp
+            L.gemm_run.argtypes = [vp, vp, vp, vp, f32, f32, vp]
+            L.gemm_run.restype = i32
+            L.gemm_run_host.argtypes = [vp, vp, vp, vp, f32, f32, vp, vp, vp, vp]
+            L.gemm_run_host.restype = i32
+            L.gemm_plan_destroy.argtypes = [vp]
+            L.gemm_plan_destroy.restype = None
+            L.gemm_plan_status.argtypes = [vp]
+            L.gemm_plan_status.restype = i32
+            L.gemm_plan_describe.argtypes = [vp]
+            L.gemm_plan_describe.restype = ctypes.c_char_p
+            L.gemm_last_error.argtypes = []
+            L.gemm_last_error.restype = ctypes.c_char_p
+            L.gemm_selftest_bounded_wait.argtypes = [ctypes.c_uint64]
+            L.gemm_selftest_bounded_wait.restype = i32
+            L.gemm_select_config.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.c_char_p, i32]
+            L.gemm_select_config.restype = i32
+            _lib = L
+    return _lib
+
+
+def _dt(dtype) -> int:
+    return DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def _p(x) -> int | None:
+    if x is None:
+        return None
+    return int(x.data_ptr()) if hasattr(x, "data_ptr") else int(x)
+
+
+def gemm_last_error() -> str:
+    return lib().gemm_last_error().decode()
+
+
+def gemm_plan_create(M: int, N: int, K: int, dtype) -> int:
+    h = lib().gemm_plan_create(M, N, K, _dt(dtype))
+    if not h:
+        raise GemmError(-1, gemm_last_error())
+    return h
+
+
+def gemm_plan_create_config(M: int, N: int, K: int, dtype, config: str | None) -> int:
+    h = lib().gemm_plan_create_config(M, N, K, _dt(dtype), config.encode() if config else None)
+    if not h:
+        raise GemmError(-1, gemm_last_error())
+    return h
+
+
+def gemm_run(plan: int, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> int:
+    return lib().gemm_run(plan, _p(A), _p(B), _p(C), alpha, beta, _p(stream))
+
+
+def gemm_run_host(plan: int, hA, hB, hC, alpha, beta, dA, dB, dC, stream=None) -> int:
+    return lib().gemm_run_host(plan, _p(hA), _p(hB), _p(hC), alpha, beta, _p(dA), _p(dB), _p(dC), _p(stream))
+
+
+def gemm_plan_destroy(plan: int) -> None:
+    lib().gemm_plan_destroy(plan)
+
+
+def gemm_plan_status(plan: int) -> int:
+    return lib().gemm_plan_status(plan)
+
+
+def gemm_plan_describe(plan: int) -> str:
+    return lib().gemm_plan_describe(plan).decode()
+
+
+def gemm_selftest_bounded_wait(timeout_ns: int) -> int:
+    return lib().gemm_selftest_bounded_wait(timeout_ns)
+
+
+def gemm_select_config(M: int, N: int, K: int, dtype, sm_count: int, tma_ok: bool) -> str:
+    buf = ctypes.create_string_buffer(64)
+    check(lib().gemm_select_config(M, N, K, _dt(dtype), sm_count, int(bool(tma_ok)), buf, 64))
+    return buf.value.decode()
+
+
+def check(status: int) -> None:
+    """Raise GemmError for a non-zero status."""
+    if status != 0:
+        raise GemmError(status, gemm_last_error())
+
+
+class Plan:
+    """Owns one gemm_plan; ``run`` takes device tensors (or raw pointers)."""
+
+    def __init__(self, M: int, N: int, K: int, dtype, config: str | None = None):
+        self.M, self.N, self.K, self.dtype = M, N, K, dtype
+        self.handle = gemm_plan_create_config(M, N, K, dtype, config)
+
+    def run(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+        check(gemm_run(self.handle, A, B, C, alpha, beta, stream))
+
+    def status(self) -> int:
+        return gemm_plan_status(self.handle)
+
+    def describe(self) -> str:
+        return gemm_plan_describe(self.handle)
+
+    def close(self) -> None:
+        if self.handle:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

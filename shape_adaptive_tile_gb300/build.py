@@ -1,0 +1,104 @@
+"""Builds the CUDA library ``_lib/libsatgemm.so`` in-tree with nvcc for sm_103a.
+
+Translation units compile in parallel; the previous library is deleted
+before linking, so a failed build never leaves a stale one behind, and a
+stamp records the nvcc version and flags, so a toolchain or flag change
+forces a rebuild.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import hashlib
+import os
+import shutil
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_DIR = os.path.join(HERE, "_lib")
+LIB = os.path.join(LIB_DIR, "libsatgemm.so")
+STAMP = os.path.join(LIB_DIR, "libsatgemm.stamp")
+
+SOURCES = ["api.cu", "aux_kernels.cu", "dispatch.cpp", "kernels_tf32.cu", "kernels_bf16.cu", "kernels_fp16.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
+
+
+def _nvcc() -> str:
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found")
+    return cand
+
+
+def _inputs():
+    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
+    files.append(os.path.join(INCLUDE, "gemm.h"))
+    return [f for f in files if os.path.isfile(f)]
+
+
+def source_hash() -> str:
+    """SHA-256 of the kernel and ABI sources (what a profile was taken of)."""
+    h = hashlib.sha256()
+    for f in _inputs():
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _key(nvcc: str) -> str:
+    ver = subprocess.run([nvcc, "--version"], capture_output=True, text=True, check=True).stdout
+    h = hashlib.sha256()
+    h.update(ver.encode())
+    h.update(" ".join(FLAGS).encode())
+    for f in _inputs():
+        with open(f, "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -> str:
+    """Compile (if needed) and return the path of the shared library."""
+    nvcc = _nvcc()
+    key = _key(nvcc)
+    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
+        with open(STAMP) as f:
+            if f.read().strip() == key:
+                return LIB
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(LIB_DIR, exist_ok=True)
+    for stale in (LIB, STAMP):
+        if os.path.exists(stale):
+            os.remove(stale)
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        if os.path.exists(obj):
+            os.remove(obj)
+        cmd = [nvcc, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose and (r.stdout or r.stderr):
+            print(r.stdout + r.stderr)
+        return obj
+
+    jobs = jobs or min(len(SOURCES), os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(key + "\n")
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

@@ -1,0 +1,422 @@
+// Host side of the C ABI declared in include/gemm.h: plan creation (device
+// checks, dispatcher, kernel preparation), tensor-map encoding and launch.
+#include "gemm.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "dispatch.h"
+#include "registry.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int elem_size(int dt) { return dt == sat::kDtTF32 ? 4 : 2; }
+
+const char* dt_name(int dt) { return dt == 0 ? "tf32" : dt == 1 ? "bf16" : "fp16"; }
+
+// 2-D row-major tensor map with a 128-byte-swizzled box of box_inner x
+// box_outer elements; out-of-bounds elements of a box read as zero.
+int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer, CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available from the driver");
+    const CUtensorMapDataType t = dt == sat::kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dt == sat::kDtBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_size(dt))};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return 0;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(GEMM_ERR_LAUNCH, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+struct gemm_plan {
+    int64_t M = 0, N = 0, K = 0;
+    int dt = 0;
+    int device = 0;
+    int sm_count = 0;
+    sat::Choice choice{};
+    bool force_plain = false;
+    const sat::KernelEntry* tma = nullptr;    // null when the strides rule out TMA
+    const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
+    int grid_tma = 0, grid_plain = 0;
+    uint32_t* d_err = nullptr;
+    unsigned long long timeout_ns = 2000000000ull;
+    char desc[256] = "";
+    mutable std::mutex mu;
+    mutable const void* map_A = nullptr;
+    mutable const void* map_B = nullptr;
+    mutable CUtensorMap tmA{}, tmB{};
+};
+
+namespace {
+
+int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
+{
+    const int64_t tm = 128 * e->cg;
+    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn);
+    int64_t slots = p->sm_count / e->cg;
+    if (e->cg == 2) {
+        // Not every SM need be able to pair with a neighbour: ask the
+        // occupancy calculator how many CTA pairs can be resident at once.
+        const int n = e->max_clusters();
+        if (n > 0 && n < slots)
+            slots = n;
+    }
+    if (slots < 1)
+        slots = 1;
+    return static_cast<int>((tiles < slots ? tiles : slots) * e->cg);
+}
+
+gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config)
+{
+    g_err[0] = '\0';
+    const int dt = static_cast<int>(dtype);
+    if (M < 0 || N < 0 || K < 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) {
+        fail(GEMM_ERR_ARG, "dimensions must be in [0, 2^31): M=%lld N=%lld K=%lld", (long long)M, (long long)N,
+             (long long)K);
+        return nullptr;
+    }
+    if (dt < 0 || dt > 2) {
+        fail(GEMM_ERR_ARG, "unknown dtype %d", dt);
+        return nullptr;
+    }
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "querying the device");
+        return nullptr;
+    }
+    if (major != 10 || minor != 3) {
+        fail(GEMM_ERR_ARCH, "device %d is compute capability %d.%d; this library is built for sm_103a only", dev,
+             major, minor);
+        return nullptr;
+    }
+    gemm_plan* p = new (std::nothrow) gemm_plan;
+    if (!p) {
+        fail(GEMM_ERR_NOMEM, "out of host memory");
+        return nullptr;
+    }
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dt = dt;
+    p->device = dev;
+    p->sm_count = sms;
+    const int64_t es = elem_size(dt);
+    const bool tma_ok = (K * es) % 16 == 0 && (N * es) % 16 == 0;
+
+    const char* source = "rule";
+    if (config && config[0]) {
+        char head[64];
+        std::snprintf(head, sizeof head, "%s", config);
+        char* plain_tag = std::strstr(head, ",plain");
+        if (plain_tag) {
+            *plain_tag = '\0';
+            p->force_plain = true;
+        }
+        if (!sat::parse_choice(head, &p->choice)) {
+            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (want \"bn,cg,raster,group[,plain]\")", config);
+            delete p;
+            return nullptr;
+        }
+        source = "forced";
+    } else {
+        p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
+        source = p->choice.source == 1 ? "table" : "rule";
+    }
+    const sat::Choice& c = p->choice;
+    if (tma_ok && !p->force_plain) {
+        p->tma = sat::find_entry(dt, c.bn, c.cg, sat::kProdTMA);
+        if (!p->tma) {
+            fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d", c.bn, c.cg);
+            delete p;
+            return nullptr;
+        }
+    }
+    p->plain = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
+    if (!p->plain) {
+        fail(GEMM_ERR_ARG, "no compiled plain-load kernel for bn=%d", c.bn);
+        delete p;
+        return nullptr;
+    }
+    for (const sat::KernelEntry* k : {p->tma, p->plain}) {
+        if (!k)
+            continue;
+        e = k->prepare();
+        if (e != cudaSuccess) {
+            cuda_fail(e, "setting the kernel's shared-memory limit");
+            delete p;
+            return nullptr;
+        }
+    }
+    if (p->tma)
+        p->grid_tma = grid_for(p, p->tma);
+    p->grid_plain = grid_for(p, p->plain);
+    e = cudaMalloc(&p->d_err, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        cuda_fail(e, "allocating the device error word");
+        if (p->d_err)
+            cudaFree(p->d_err);
+        delete p;
+        return nullptr;
+    }
+    if (const char* t = std::getenv("SAT_GEMM_WAIT_TIMEOUT_MS")) {
+        const long long ms = std::atoll(t);
+        if (ms > 0)
+            p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+    const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d grid%d %s",
+                  dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
+                  p->tma ? "tma" : "plain", c.raster, c.group, p->tma ? p->grid_tma : p->grid_plain, source);
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
+{
+    return create(M, N, K, dtype, nullptr);
+}
+
+gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config)
+{
+    return create(M, N, K, dtype, config);
+}
+
+void gemm_plan_destroy(gemm_plan* plan)
+{
+    if (!plan)
+        return;
+    if (plan->d_err)
+        cudaFree(plan->d_err);
+    delete plan;
+}
+
+const char* gemm_plan_describe(const gemm_plan* plan) { return plan ? plan->desc : ""; }
+
+const char* gemm_last_error(void) { return g_err; }
+
+int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float alpha, float beta, void* cuda_stream)
+{
+    if (!p)
+        return fail(GEMM_ERR_ARG, "plan is NULL");
+    if (p->M == 0 || p->N == 0)
+        return GEMM_OK;
+    if (!C)
+        return fail(GEMM_ERR_ARG, "C is NULL");
+    if (reinterpret_cast<uintptr_t>(C) % 4 != 0)
+        return fail(GEMM_ERR_ALIGN, "C must be 4-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev != p->device)
+        return fail(GEMM_ERR_ARG, "plan was made for device %d but device %d is current", p->device, dev);
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    if (p->K == 0 || alpha == 0.0f) {
+        e = sat::launch_scale(C, static_cast<long long>(p->M * p->N), beta, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the beta-scale kernel");
+    }
+    if (!A || !B)
+        return fail(GEMM_ERR_ARG, "A or B is NULL");
+    const uintptr_t es = static_cast<uintptr_t>(elem_size(p->dt));
+    if (reinterpret_cast<uintptr_t>(A) % es || reinterpret_cast<uintptr_t>(B) % es)
+        return fail(GEMM_ERR_ALIGN, "A and B must be aligned to their %d-byte element size", (int)es);
+    const bool use_tma =
+        p->tma && reinterpret_cast<uintptr_t>(A) % 16 == 0 && reinterpret_cast<uintptr_t>(B) % 16 == 0;
+    const sat::KernelEntry* k = use_tma ? p->tma : p->plain;
+
+    sat::GemmArgs a{};
+    a.M = static_cast<int>(p->M);
+    a.N = static_cast<int>(p->N);
+    a.K = static_cast<int>(p->K);
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.tiles_m = static_cast<int>((p->M + 128 * k->cg - 1) / (128 * k->cg));
+    a.tiles_n = static_cast<int>((p->N + k->bn - 1) / k->bn);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.num_kb = static_cast<int>((p->K + k->bk - 1) / k->bk);
+    a.group = p->choice.group;
+    a.raster = p->choice.raster;
+    a.err = p->d_err;
+    a.timeout_ns = p->timeout_ns;
+
+    CUtensorMap tmA{}, tmB{};
+    if (use_tma) {
+        std::lock_guard<std::mutex> lock(p->mu);
+        if (p->map_A != A) {
+            const int rc =
+                encode_2d(&p->tmA, p->dt, A, p->K, p->M, static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc) {
+                p->map_A = nullptr;
+                return rc;
+            }
+            p->map_A = A;
+        }
+        if (p->map_B != B) {
+            const int rc = encode_2d(&p->tmB, p->dt, B, p->N, p->K, static_cast<uint32_t>(128 / es),
+                                     static_cast<uint32_t>(k->bk), static_cast<CUtensorMapSwizzle>(k->b_swizzle));
+            if (rc) {
+                p->map_B = nullptr;
+                return rc;
+            }
+            p->map_B = B;
+        }
+        tmA = p->tmA;
+        tmB = p->tmB;
+    }
+    e = k->launch(&tmA, &tmB, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the GEMM kernel");
+}
+
+int gemm_run_host(const gemm_plan* p, const void* hA, const void* hB, float* hC, float alpha, float beta, void* dA,
+                  void* dB, float* dC, void* cuda_stream)
+{
+    if (!p)
+        return fail(GEMM_ERR_ARG, "plan is NULL");
+    if (p->M == 0 || p->N == 0)
+        return GEMM_OK;
+    if (!hC || !dC || (p->K > 0 && (!hA || !hB || !dA || !dB)))
+        return fail(GEMM_ERR_ARG, "NULL buffer");
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const size_t es = static_cast<size_t>(elem_size(p->dt));
+    cudaError_t e = cudaSuccess;
+    if (p->K > 0 && alpha != 0.0f) {
+        e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(p->M * p->K) * es, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(p->K * p->N) * es, cudaMemcpyHostToDevice, s);
+    }
+    const size_t cbytes = static_cast<size_t>(p->M * p->N) * sizeof(float);
+    if (e == cudaSuccess && beta != 0.0f)
+        e = cudaMemcpyAsync(dC, hC, cbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copying operands to the device");
+    const int rc = gemm_run(p, dA, dB, dC, alpha, beta, cuda_stream);
+    if (rc)
+        return rc;
+    e = cudaMemcpyAsync(hC, dC, cbytes, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "copying C to the host");
+}
+
+int gemm_plan_status(const gemm_plan* p)
+{
+    if (!p)
+        return fail(GEMM_ERR_ARG, "plan is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device error");
+    uint32_t h = 0;
+    e = cudaMemcpy(&h, p->d_err, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+        e = cudaMemset(p->d_err, 0, sizeof h);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the device error word");
+    if (h)
+        return fail(GEMM_ERR_TIMEOUT, "a bounded wait gave up inside the kernel (error bits 0x%x)", h);
+    return GEMM_OK;
+}
+
+int gemm_selftest_bounded_wait(uint64_t timeout_ns)
+{
+    if (timeout_ns > 1000000000ull)
+        timeout_ns = 1000000000ull;
+    uint32_t* d = nullptr;
+    cudaError_t e = cudaMalloc(&d, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = cudaMemset(d, 0, sizeof(uint32_t));
+    if (e == cudaSuccess)
+        e = sat::launch_wait_probe(d, timeout_ns, nullptr);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    uint32_t h = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&h, d, sizeof h, cudaMemcpyDeviceToHost);
+    if (d)
+        cudaFree(d);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "bounded-wait self-test");
+    if (h & (1u << 4))
+        return fail(GEMM_ERR_TIMEOUT, "the probe's wait gave up after its limit, as designed");
+    return fail(GEMM_ERR_LAUNCH, "the probe's wait did not report a timeout (error word 0x%x)", h);
+}
+
+int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int sm_count, int tma_ok, char* out,
+                       int out_len)
+{
+    const int dt = static_cast<int>(dtype);
+    if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
+        return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
+    const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.source == 1 ? "table" : "rule");
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Shape-adaptive choice of tile and schedule.
+//
+// "Measured data point on fixed-tile vs shape-adaptive GEMM" (section "The
+// wall, and why we think it's structural", and section 2.1 of the matching
+// post-mortem "Post-mortem: a GPU stack without nvcc, cuBLAS, or LLVM")
+// reports that one fixed 128x128 tile reaches parity in one band of shapes
+// and loses outside it, and that the schedule, not only the tile size, was
+// the binding term. The FlashInfer pull request "fix(fp4_gemm autotune) SM107
+// kernel family excluded from autotune candidates" adds that the tile count
+// against the SM count (wave quantization) and the raster order both swing
+// throughput. So the choice here covers tile N, CTA pair vs single SM,
+// raster order and raster group, in two steps:
+//   1. an exact (dtype, M, N, K) hit in the committed sweep table
+//      (sweep_table.inc, written from on-device measurements), else
+//   2. an analytic rule: estimated time = waves x per-tile time, where
+//      waves = ceil(tiles / concurrent tiles) and a tile costs the larger of
+//      its tensor-core time and its operand-fill time.
+#include "dispatch.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+namespace sat {
+
+namespace {
+
+struct TableRow {
+    int dt;
+    int64_t M, N, K;
+    Choice c;
+};
+
+const TableRow kTable[] = {
+#include "sweep_table.inc"
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+bool parse_choice(const char* spec, Choice* out)
+{
+    Choice c{};
+    if (!spec || std::sscanf(spec, "%d,%d,%d,%d", &c.bn, &c.cg, &c.raster, &c.group) != 4)
+        return false;
+    if ((c.bn != 64 && c.bn != 128 && c.bn != 256) || (c.cg != 1 && c.cg != 2) || (c.raster != 0 && c.raster != 1) ||
+        c.group < 1 || (c.cg == 2 && c.bn == 64))
+        return false;
+    c.source = 2;
+    *out = c;
+    return true;
+}
+
+Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool tma_ok)
+{
+    for (const TableRow& r : kTable) {
+        if (r.dt == dt && r.M == M && r.N == N && r.K == K && (tma_ok || r.c.cg == 1)) {
+            Choice c = r.c;
+            c.source = 1;
+            if (!tma_ok && c.bn == 64)
+                c.bn = 128;
+            return c;
+        }
+    }
+    // Analytic rule. Per-SM rates: dense tensor FLOP per clock (bf16/fp16
+    // 8192, tf32 4096) and a sustained operand-fill rate from L2 of about
+    // 64 bytes per clock per SM; the plain-load path fills far slower.
+    const double es = dt == 0 ? 4.0 : 2.0;
+    const double flop_clk = dt == 0 ? 4096.0 : 8192.0;
+    const double fill_clk = tma_ok ? 64.0 : 12.0;
+    const double epi_clk = 4096.0;  // epilogue not hidden behind the last tile
+    struct Cand { int bn, cg; };
+    const Cand cands[] = {{256, 2}, {128, 2}, {256, 1}, {128, 1}, {64, 1}};
+    double best_t = 1e300;
+    Choice best{256, 1, 0, 8, 0};
+    for (const Cand& cd : cands) {
+        if (!tma_ok && (cd.cg == 2 || cd.bn == 64))
+            continue;
+        const int64_t tm = 128 * cd.cg;
+        const int64_t tiles = cdiv(M, tm) * cdiv(N, cd.bn);
+        const int64_t slots = std::max<int64_t>(1, sm_count / cd.cg);
+        const int64_t waves = cdiv(tiles, slots);
+        // Per CTA: its MMA share and the bytes it loads per unit of K.
+        const double mma = 2.0 * 128.0 * cd.bn * K / flop_clk;
+        const double fill = (128.0 + cd.bn / cd.cg) * es * K / fill_clk;
+        const double t = waves * std::max(mma, fill) + epi_clk;
+        // Prefer the larger tile unless the smaller is clearly faster.
+        if (t < best_t * 0.97) {
+            best_t = t;
+            best.bn = cd.bn;
+            best.cg = cd.cg;
+        }
+    }
+    best.raster = 0;
+    best.group = best.cg == 2 ? 4 : 8;
+    best.source = 0;
+    return best;
+}
+
+}  // namespace sat

@@ -1,0 +1,32 @@
+// Kernel arguments shared by the host launcher and the device code.
+#pragma once
+
+#include <cstdint>
+
+namespace sat {
+
+// Operand element types (same numbering as gemm_dtype_t in gemm.h).
+constexpr int kDtTF32 = 0;
+constexpr int kDtBF16 = 1;
+constexpr int kDtFP16 = 2;
+
+// Producer kinds.
+constexpr int kProdTMA = 0;    // TMA tensor loads (16-byte aligned bases and strides)
+constexpr int kProdPlain = 1;  // plain loads into the same swizzled layout (any stride)
+
+struct GemmArgs {
+    int M, N, K;
+    const void* A;             // M x K row-major (plain-load producer only)
+    const void* B;             // K x N row-major (plain-load producer only)
+    float* C;                  // M x N row-major
+    float alpha, beta;
+    int tiles_m, tiles_n;      // tiles of (128 * cta_group) x BN
+    int num_tiles;
+    int num_kb;                // ceil(K / BK)
+    int group;                 // rasterisation group size (>= 1)
+    int raster;                // 0: groups along M, 1: groups along N
+    uint32_t* err;             // device error word (bounded-wait timeouts), may be null
+    unsigned long long timeout_ns;
+};
+
+}  // namespace sat

@@ -1,0 +1,479 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:
+//     C[M x N] = alpha * A[M x K] * B[K x N] + beta * C      (row-major, fp32 C)
+//
+// This is the fixed-schedule kernel that "Measured data point on fixed-tile
+// vs shape-adaptive GEMM" (section "The wall, and why we think it's
+// structural") says is not enough on its own, re-done for Blackwell: every
+// instantiation is one (tile, schedule) point among which the shape-adaptive
+// dispatcher chooses.
+//
+// Roles (one CTA per SM, or a CTA pair on two SMs for cta_group::2):
+//   producer warp(s): fill an S-stage shared-memory ring, by TMA (2-D tiled
+//       loads, 128-byte swizzle, zero fill outside the matrix) or, when a row
+//       stride is not a multiple of 16 bytes, by plain loads written into the
+//       same swizzled layout;
+//   MMA warp: one thread issues tcgen05.mma (kind::tf32 or kind::f16) from
+//       the ring into a TMEM accumulator, releasing each stage with
+//       tcgen05.commit; two accumulators alternate so that the epilogue of one
+//       tile overlaps the main loop of the next;
+//   4 epilogue warps: tcgen05.ld TMEM -> registers, transpose through a
+//       per-warp shared buffer, then alpha*acc (+ beta*C) with row-contiguous,
+//       masked stores (no alignment needed, any M/N tail).
+// The K loop always runs k = 0..K-1 in the same order for a tile, and no
+// output element is produced by more than one CTA, so results are
+// bit-identical from run to run.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+#include <cuda.h>
+
+#include "gemm_args.h"
+#include "ptx.cuh"
+
+namespace sat {
+
+// Error bits written to the device error word.
+constexpr uint32_t kErrTimeoutProducer = 1u << 0;
+constexpr uint32_t kErrTimeoutMma = 1u << 1;
+constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
+constexpr uint32_t kErrTimeoutDrain = 1u << 3;
+
+template <int DT, int BN, int CG, int PROD>
+struct Traits {
+    static constexpr bool kTF32 = DT == kDtTF32;
+    static constexpr int ES = kTF32 ? 4 : 2;        // bytes per operand element
+    static constexpr int BM = 128;                  // accumulator rows per CTA
+    static constexpr int BK = 128 / ES;             // one 128-byte swizzle row of K
+    static constexpr int UK = 32 / ES;              // K of one MMA instruction
+    static constexpr int KSTEPS = BK / UK;
+    static constexpr int CW = 128 / ES;             // B columns per swizzle row
+    static constexpr int BN_CTA = BN / CG;          // B columns this CTA loads
+    static constexpr int NBOX = BN_CTA / CW;        // B boxes per stage
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = NBOX * BK * 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_FLOATS = 32 * 33;      // per epilogue warp
+    static constexpr int EPI_BYTES = 4 * EPI_FLOATS * 4;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
+    static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int NPW = PROD == kProdTMA ? 1 : 4;   // producer warps
+    static constexpr int MMA_WARP = NPW;
+    static constexpr int EPI_WARP0 = NPW + 1;
+    static constexpr int THREADS = (NPW + 1 + 4) * 32;
+    static constexpr int ACC_COLS = BN;             // fp32 accumulator: one column per element
+    static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+    static constexpr uint32_t FMT = DT == kDtTF32 ? kFmtTF32 : DT == kDtBF16 ? kFmtBF16 : kFmtF16;
+    // B in shared memory. TMA copies B as it lies in memory (N contiguous,
+    // "MN-major"); 16-bit types use the 128-byte swizzle, 32-bit (tf32)
+    // types the 128-byte swizzle with 32-byte atoms, the only MN-major
+    // swizzle the tensor core takes for 32-bit operands. The plain-load
+    // producer of tf32 instead stores B transposed, K-major like A.
+    static constexpr bool B_MN = !(kTF32 && PROD == kProdPlain);
+    static constexpr uint32_t B_LAYOUT = (kTF32 && B_MN) ? kLayoutSW128Atom32 : kLayoutSW128;
+    static constexpr uint32_t IDESC = idesc_f32acc(FMT, BM * CG, BN, B_MN);
+    // MN-major: 128-byte column blocks are BK*128 bytes apart (leading byte
+    // offset); K rows come in swizzle groups, 8 rows (1024 bytes) for the
+    // 16-byte-atom swizzle and 4 rows (512 bytes) for the 32-byte-atom one
+    // (stride byte offset); one MMA step of K advances UK rows of 128 bytes.
+    // K-major: rows of 128 bytes, 8-row groups 1024 bytes apart, and one step
+    // of K advances 32 bytes inside the swizzled row.
+    static constexpr uint32_t B_LBO = B_MN ? BK * 128 : 16;
+    static constexpr uint32_t B_SBO = B_LAYOUT == kLayoutSW128Atom32 ? 512 : 1024;
+    static constexpr uint32_t B_KSTEP = B_MN ? UK * 128 : UK * ES;
+    static constexpr uint32_t A_KSTEP = UK * ES;    // bytes per MMA step of K in A (= 32)
+
+    static_assert(BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
+    static_assert(BN >= 16 && BN <= 256 && BN % 16 == 0, "MMA N");
+    static_assert(STAGES >= 2, "ring too small");
+    static_assert(PROD == kProdTMA || CG == 1, "plain-load producer is 1-SM only");
+    static_assert(2 * BN <= 512, "two accumulators must fit in TMEM");
+};
+
+__device__ __forceinline__ void tile_coord(int t, const GemmArgs& a, int& tm, int& tn)
+{
+    if (a.raster == 0) {  // groups of `group` tile-rows, rows fastest inside a group
+        const int per = a.group * a.tiles_n;
+        const int g = t / per, r = t - g * per;
+        const int first = g * a.group;
+        const int gs = min(a.group, a.tiles_m - first);
+        tm = first + r % gs;
+        tn = r / gs;
+    } else {              // groups of `group` tile-columns, columns fastest
+        const int per = a.group * a.tiles_m;
+        const int g = t / per, r = t - g * per;
+        const int first = g * a.group;
+        const int gs = min(a.group, a.tiles_n - first);
+        tn = first + r % gs;
+        tm = r / gs;
+    }
+}
+
+// Byte offset of operand element (row r, k) in a K-major 128-byte-swizzled
+// tile: 16-byte chunk index XOR (row mod 8), rows 128 bytes apart.
+template <int ES>
+__device__ __forceinline__ uint32_t swz_kmajor(int r, int k)
+{
+    const uint32_t kb = static_cast<uint32_t>(k * ES);
+    return static_cast<uint32_t>(r) * 128u + ((((kb >> 4) ^ static_cast<uint32_t>(r & 7)) << 4) | (kb & 15u));
+}
+
+// Byte offset of B element (k, n) in the MN-major tile: column blocks of
+// 128 bytes, each BK rows of 128 bytes with the same XOR swizzle.
+template <int ES, int BK>
+__device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
+{
+    constexpr int CW = 128 / ES;
+    const int j = n / CW, nn = n - j * CW;
+    const uint32_t nb = static_cast<uint32_t>(nn * ES);
+    return static_cast<uint32_t>(j * BK * 128 + k * 128) +
+           ((((nb >> 4) ^ static_cast<uint32_t>(k & 7)) << 4) | (nb & 15u));
+}
+
+template <int DT, int BN, int CG, int PROD>
+__global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
+    sat_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs args)
+{
+    using T = Traits<DT, BN, CG, PROD>;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Shared-memory carve-up (identical in both CTAs of a pair).
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + T::STAGES * T::A_BYTES;
+    float* const epi = reinterpret_cast<float*>(gbase + T::STAGES * T::STAGE_BYTES);
+    const uint32_t bars = base + T::STAGES * T::STAGE_BYTES + T::EPI_BYTES;
+    uint8_t* const gbars = gbase + T::STAGES * T::STAGE_BYTES + T::EPI_BYTES;
+    // barrier slots (8 bytes each)
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (T::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * T::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * T::STAGES + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * T::STAGES + 4);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 8 * (2 * T::STAGES + 5));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 8 * (2 * T::STAGES + 5) + 4);
+
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(full_bar(s), PROD == kProdTMA ? CG : T::NPW * 32);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4 * CG);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (PROD == kProdTMA && warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == T::MMA_WARP) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), T::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
+    constexpr bool kClu = CG == 2;
+    const int tile_step = gridDim.x / CG;
+    const int tile0 = blockIdx.x / CG;
+
+    if (warp < T::NPW) {
+        // ------------------------------------------------------------ producer
+        if constexpr (PROD == kProdTMA) {
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                // The pair's loads all complete on the leader's barrier.
+                const uint32_t full0 = CG == 2 ? map_to_cta(full_bar(0), 0) : full_bar(0);
+                for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+                    int tm, tn;
+                    tile_coord(t, args, tm, tn);
+                    const int m0 = tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
+                    const int n0 = tn * BN + static_cast<int>(rank) * T::BN_CTA;
+                    for (int kb = 0; kb < args.num_kb; ++kb) {
+                        if (!wait_bar<kClu>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = full0 + 8u * stage;
+                        const int k0 = kb * T::BK;
+                        if constexpr (CG == 1) {
+                            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
+                            tma_load_2d(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
+#pragma unroll
+                            for (int j = 0; j < T::NBOX; ++j)
+                                tma_load_2d(sB + stage * T::B_BYTES + j * (T::BK * 128), &tmB, fb, n0 + j * T::CW, k0);
+                        } else {
+                            mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
+                            tma_load_2d_pair(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
+#pragma unroll
+                            for (int j = 0; j < T::NBOX; ++j)
+                                tma_load_2d_pair(sB + stage * T::B_BYTES + j * (T::BK * 128), &tmB, fb,
+                                                 n0 + j * T::CW, k0);
+                        }
+                        if (++stage == T::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                // Drain: wait until the MMA has released every stage filled
+                // above, so no copy or commit is in flight when the CTA ends.
+                if (ok) {
+                    for (int i = 0; i < T::STAGES; ++i) {
+                        if (!wait_bar<kClu>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer))
+                            break;
+                        if (++stage == T::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+        } else {
+            // Plain-load producer (1-SM): any row stride, 2- or 4-byte aligned.
+            using E = typename std::conditional<T::kTF32, uint32_t, uint16_t>::type;
+            const E* __restrict__ gA = static_cast<const E*>(args.A);
+            const E* __restrict__ gB = static_cast<const E*>(args.B);
+            constexpr int NP = T::NPW * 32;
+            constexpr int BATCH = 16;
+            const int p = threadIdx.x;  // producer warps are warps 0..NPW-1
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+                int tm, tn;
+                tile_coord(t, args, tm, tn);
+                const int m0 = tm * T::BM;
+                const int n0 = tn * BN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k0 = kb * T::BK;
+                    uint8_t* const dA = gbase + (sA - base) + stage * T::A_BYTES;
+                    uint8_t* const dB = gbase + (sB - base) + stage * T::B_BYTES;
+                    // A tile: BM x BK, consecutive threads take consecutive k.
+                    constexpr int NA = T::BM * T::BK / NP;
+                    static_assert(NA % BATCH == 0, "A batch");
+#pragma unroll 1
+                    for (int i0 = 0; i0 < NA; i0 += BATCH) {
+                        E v[BATCH];
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int idx = p + (i0 + i) * NP;
+                            const int r = idx / T::BK, k = idx - r * T::BK;
+                            const int gm = m0 + r, gk = k0 + k;
+                            v[i] = (gm < args.M && gk < args.K) ? __ldg(gA + static_cast<int64_t>(gm) * args.K + gk)
+                                                                : E(0);
+                        }
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int idx = p + (i0 + i) * NP;
+                            const int r = idx / T::BK, k = idx - r * T::BK;
+                            *reinterpret_cast<E*>(dA + swz_kmajor<T::ES>(r, k)) = v[i];
+                        }
+                    }
+                    // B tile: BK x BN, consecutive threads take consecutive n.
+                    constexpr int NB = T::BK * BN / NP;
+                    static_assert(NB % BATCH == 0, "B batch");
+#pragma unroll 1
+                    for (int i0 = 0; i0 < NB; i0 += BATCH) {
+                        E v[BATCH];
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int idx = p + (i0 + i) * NP;
+                            const int kr = idx / BN, n = idx - kr * BN;
+                            const int gk = k0 + kr, gn = n0 + n;
+                            v[i] = (gk < args.K && gn < args.N) ? __ldg(gB + static_cast<int64_t>(gk) * args.N + gn)
+                                                                : E(0);
+                        }
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int idx = p + (i0 + i) * NP;
+                            const int kr = idx / BN, n = idx - kr * BN;
+                            if constexpr (T::B_MN)
+                                *reinterpret_cast<E*>(dB + swz_mnmajor<T::ES, T::BK>(kr, n)) = v[i];
+                            else
+                                *reinterpret_cast<E*>(dB + swz_kmajor<T::ES>(n, kr)) = v[i];
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(full_bar(stage));
+                    if (++stage == T::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok) {
+                for (int i = 0; i < T::STAGES; ++i) {
+                    if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer))
+                        break;
+                    if (++stage == T::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == T::MMA_WARP) {
+        // ----------------------------------------------------------------- MMA
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true, issued = false;
+            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+                if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!wait_bar<kClu>(full_bar(stage), phase, wc, kErrTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * T::A_BYTES;
+                    const uint32_t b0 = sB + stage * T::B_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < T::KSTEPS; ++ks) {
+                        const uint64_t ad = sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
+                        const uint64_t bd = sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
+                        mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    if constexpr (CG == 1)
+                        mma_commit(empty_bar(stage));
+                    else
+                        mma_commit_pair(empty_bar(stage), 0x3);
+                    if (++stage == T::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                if constexpr (CG == 1)
+                    mma_commit(tfull_bar(acc));
+                else
+                    mma_commit_pair(tfull_bar(acc), 0x3);
+                acc ^= 1;
+                if (acc == 0)
+                    acc_phase ^= 1u;
+            }
+            if (!ok && issued) {
+                // Let issued MMAs finish before tensor memory is freed.
+                if constexpr (CG == 1)
+                    mma_commit(drain_bar);
+                else
+                    mma_commit_pair(drain_bar, 0x1);
+                const WaitCtl dw{abort_flag, args.err, args.timeout_ns};
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait<kClu>(drain_bar, 0)) {
+                    if (globaltimer_ns() - t0 > dw.timeout_ns) {
+                        if (args.err)
+                            atomicOr(args.err, kErrTimeoutDrain);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - T::EPI_WARP0;      // 0..3
+        const int sub = warp & 3;                // TMEM lane quarter this warp may access
+        float* const buf = epi + ew * T::EPI_FLOATS;
+        const uint32_t tempty0 = CG == 2 ? map_to_cta(tempty_bar(0), 0) : tempty_bar(0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const float alpha = args.alpha, beta = args.beta;
+        const int64_t ldc = args.N;
+        for (int t = tile0; t < args.num_tiles; t += tile_step) {
+            if (!wait_bar<kClu>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
+                break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coord(t, args, tm, tn);
+            const int row0 = tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
+            const int n0 = tn * BN;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
+                                   static_cast<uint32_t>(acc * T::ACC_COLS);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, r);
+                tmem_wait_ld();
+                if (c == BN / 32 - 1) {
+                    // All TMEM reads of this accumulator are done: hand it back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1)
+                            mbar_arrive(tempty0 + 8u * acc);
+                        else
+                            mbar_arrive_cluster(tempty0 + 8u * acc);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    buf[lane * 33 + j] = __uint_as_float(r[j]);
+                __syncwarp();
+                const int col = n0 + c * 32 + lane;
+                if (col < args.N) {
+                    float* cp = args.C + static_cast<int64_t>(row0) * ldc + col;
+                    const int rows = min(32, args.M - row0);
+#pragma unroll 4
+                    for (int i = 0; i < rows; ++i) {
+                        float v = alpha * buf[i * 33 + lane];
+                        if (beta != 0.0f)
+                            v = fmaf(beta, cp[i * ldc], v);
+                        cp[i * ldc] = v;
+                    }
+                }
+                __syncwarp();
+            }
+            acc ^= 1;
+            if (acc == 0)
+                acc_phase ^= 1u;
+        }
+    }
+
+    // ------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync();
+    if (warp == T::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc<CG>(tmem_base, T::TMEM_COLS);
+    }
+}
+
+}  // namespace sat

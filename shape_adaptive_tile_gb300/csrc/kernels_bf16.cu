@@ -1,0 +1,9 @@
+// Kernel variants for bf16 operands.
+#include "launch.cuh"
+
+namespace sat {
+
+const KernelEntry kEntriesBF16[] = {SAT_ENTRIES(kDtBF16)};
+const int kNumEntriesBF16 = sizeof(kEntriesBF16) / sizeof(kEntriesBF16[0]);
+
+}  // namespace sat

@@ -1,0 +1,9 @@
+// Kernel variants for tf32 operands.
+#include "launch.cuh"
+
+namespace sat {
+
+const KernelEntry kEntriesTF32[] = {SAT_ENTRIES(kDtTF32)};
+const int kNumEntriesTF32 = sizeof(kEntriesTF32) / sizeof(kEntriesTF32[0]);
+
+}  // namespace sat

@@ -1,0 +1,43 @@
+// Table of compiled kernel variants, one entry per (dtype, BN, cta_group,
+// producer). The dispatcher picks among these; the launcher runs one.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_args.h"
+
+namespace sat {
+
+struct KernelEntry {
+    int dt;        // kDtTF32 / kDtBF16 / kDtFP16
+    int bn;        // N of the output tile
+    int cg;        // 1: one SM per 128-row tile; 2: a CTA pair (cluster of 2) per 256-row tile
+    int prod;      // kProdTMA / kProdPlain
+    int stages;    // shared-memory ring depth
+    int threads;   // CTA size
+    int smem;      // dynamic shared memory bytes
+    int bk;        // K per stage
+    int b_swizzle; // CUtensorMapSwizzle of B's tensor map
+    cudaError_t (*prepare)();  // sets the kernel's dynamic shared-memory limit
+    int (*max_clusters)();     // co-resident CTA pairs on this device (cg == 2), 0 if unknown
+    cudaError_t (*launch)(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs* args, int grid,
+                          cudaStream_t stream);
+};
+
+// Defined in kernels_<dtype>.cu.
+extern const KernelEntry kEntriesTF32[];
+extern const int kNumEntriesTF32;
+extern const KernelEntry kEntriesBF16[];
+extern const int kNumEntriesBF16;
+extern const KernelEntry kEntriesFP16[];
+extern const int kNumEntriesFP16;
+
+// Finds the variant, or nullptr.
+const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
+
+// Defined in aux_kernels.cu.
+cudaError_t launch_scale(float* C, long long n, float beta, cudaStream_t stream);
+cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
+
+}  // namespace sat

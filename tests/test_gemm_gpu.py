@@ -1,0 +1,164 @@
+"""GPU parity of every kernel variant against the FP64 oracle, through the C ABI.
+
+Small shapes (several tiles in each dimension plus ragged M/N/K tails) are
+compared element by element with the oracle: bit-exact on the dyadic
+family (every product and partial sum is exact in fp32, so exactly one
+result is correct), rel_rms within the dtype's bound on Gaussian inputs.
+Every configuration the dispatcher can choose is forced in turn, including
+CTA pairs, both raster orders and the plain-load producer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shape_adaptive_tile_gb300 as sat
+import synth_inputs as si
+from tests import checks
+from tests.gpu_util import run, run_np, stream, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["tf32", "bf16", "fp16"]
+# bn, cg, raster, group[, plain]
+CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,2,1,1",
+           "256,1,0,8,plain", "128,1,1,3,plain"]
+SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    sat.build()
+    sat.lib()
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_config_dyadic_bit_exact(dtype, config):
+    for i, (M, N, K) in enumerate(SHAPES):
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 100 + i, "dyadic")
+        _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+        checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_config_normal_rel_rms(dtype, config):
+    M, N, K = 333, 517, 389
+    A, B, C0 = si.problem(M, N, K, dtype, "normal", 5, "normal")
+    ref64, _ = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+    checks.assert_rel_rms(got, ref64, si.REL_RMS_BOUND[dtype], f"{dtype} [{desc}]")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_beta_zero_ignores_nan_c(dtype):
+    M, N, K = 200, 300, 100
+    A, B, _ = si.problem(M, N, K, dtype, "dyadic", 9)
+    _, ref32 = oracle.gemm(A, B, None, 2.0, 0.0, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, None, 2.0, 0.0)   # C starts all NaN
+    checks.assert_bit_exact(got, ref32, desc)
+
+
+def test_k_zero_and_alpha_zero_scale_c():
+    M, N = 70, 90
+    C0 = si.c_matrix("normal", M, N, 3)
+    for K, alpha in ((0, 1.0), (16, 0.0)):
+        A = np.zeros((M, K), np.float32)
+        B = np.zeros((K, N), np.float32)
+        got, _ = run_np(M, N, K, "tf32", A, B, C0, alpha, 0.25)
+        assert np.array_equal(got, (0.25 * C0.astype(np.float64)).astype(np.float32))
+    # beta == 0 with K == 0 zeroes C, NaN included
+    got, _ = run_np(M, N, 0, "tf32", np.zeros((M, 0), np.float32), np.zeros((0, N), np.float32), None, 1.0, 0.0)
+    assert np.all(got == 0.0)
+
+
+def test_empty_m_or_n_is_a_no_op():
+    for M, N in ((0, 5), (5, 0)):
+        with sat.Plan(M, N, 8, "bf16") as plan:
+            plan.run(0, 0, 0, 1.0, 0.0, stream())
+            torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_misaligned_pointers_take_the_plain_path(dtype):
+    """Operands that start one element past a 16-byte boundary cannot be
+    described by a TMA tensor map; the plan switches to the plain-load
+    producer and must give the same bits."""
+    M, N, K = 150, 264, 96      # row strides 16-byte multiples: TMA-able when aligned
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 12, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.0, 1.0, dtype)
+    es = 4 if dtype == "tf32" else 2
+    flatA = to_dev(np.concatenate([np.zeros(1, A.dtype), A.ravel()]), dtype)
+    flatB = to_dev(np.concatenate([np.zeros(1, B.dtype), B.ravel()]), dtype)
+    dC = to_dev(C0)
+    with sat.Plan(M, N, K, dtype) as plan:
+        assert "tma" in plan.describe()
+        run(plan, flatA.data_ptr() + es, flatB.data_ptr() + es, dC, 1.0, 1.0)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    checks.assert_bit_exact(dC.cpu().numpy(), ref32, "misaligned")
+
+
+def test_error_codes():
+    with pytest.raises(sat.GemmError):
+        sat.gemm_plan_create(-1, 4, 4, "tf32")
+    with pytest.raises(sat.GemmError):
+        sat.gemm_plan_create(4, 4, 4, 7)
+    with pytest.raises(sat.GemmError):
+        sat.gemm_plan_create_config(4, 4, 4, "tf32", "96,1,0,8")
+    h = sat.gemm_plan_create(64, 64, 64, "bf16")
+    try:
+        x = torch.zeros(64 * 64 + 1, dtype=torch.bfloat16, device="cuda")
+        c = torch.zeros(64 * 64 + 1, dtype=torch.float32, device="cuda")
+        assert sat.gemm_run(h, None, x, c, 1.0, 0.0, stream()) == -1
+        assert sat.gemm_run(h, x.data_ptr() + 1, x, c, 1.0, 0.0, stream()) == -3   # odd address
+        assert sat.gemm_run(h, x, x, c.data_ptr() + 2, 1.0, 0.0, stream()) == -3   # C not 4-aligned
+        assert sat.gemm_run(None, x, x, c, 1.0, 0.0, stream()) == -1
+        assert "aligned" in sat.gemm_last_error() or "NULL" in sat.gemm_last_error()
+    finally:
+        sat.gemm_plan_destroy(h)
+    sat.gemm_plan_destroy(None)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    assert sat.gemm_selftest_bounded_wait(20_000_000) == -5
+    # The context is still usable: a GEMM runs and is exact afterwards.
+    A, B, _ = si.problem(64, 64, 64, "bf16", "dyadic", 1)
+    _, ref32 = oracle.gemm(A, B, None, 1.0, 0.0, "bf16")
+    got, _ = run_np(64, 64, 64, "bf16", A, B, None, 1.0, 0.0)
+    checks.assert_bit_exact(got, ref32, "after timeout self-test")
+
+
+def test_run_host_end_to_end():
+    M, N, K = 257, 129, 70
+    A, B, C0 = si.problem(M, N, K, "fp16", "dyadic", 13, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 0.5, 1.5, "fp16")
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.from_numpy(C0.copy()).pin_memory()
+    dA = torch.empty_like(hA, device="cuda")
+    dB = torch.empty_like(hB, device="cuda")
+    dC = torch.empty_like(hC, device="cuda")
+    with sat.Plan(M, N, K, "fp16") as plan:
+        sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, 0.5, 1.5, dA, dB, dC, stream()))
+        torch.cuda.synchronize()
+    checks.assert_bit_exact(hC.numpy(), ref32, "gemm_run_host")
+
+
+def test_plan_runs_on_two_streams():
+    M, N, K = 384, 512, 256
+    A, B, _ = si.problem(M, N, K, "bf16", "dyadic", 14)
+    _, ref32 = oracle.gemm(A, B, None, 1.0, 0.0, "bf16")
+    dA, dB = to_dev(A, "bf16"), to_dev(B, "bf16")
+    outs = [torch.empty(M, N, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    with sat.Plan(M, N, K, "bf16") as plan:
+        for s, c in zip(streams, outs):
+            sat.check(sat.gemm_run(plan.handle, dA, dB, c, 1.0, 0.0, s.cuda_stream))
+        torch.cuda.synchronize()
+    for c in outs:
+        checks.assert_bit_exact(c.cpu().numpy(), ref32, "two streams")
