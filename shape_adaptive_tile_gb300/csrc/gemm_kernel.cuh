@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::STAGES; ++s) {
-            mbar_init(full_bar(s), PROD == kProdTMA ? CG : T::NPW * 32);
+            mbar_init(full_bar(s), PROD == kProdTMA ? 1 : T::NPW * 32);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
+    // Barriers completed by TMA transactions or tcgen05.commit need only
+    // CTA-scope acquire; the one barrier that the peer CTA's epilogue
+    // arrives on with plain arrives (TMEM released) needs cluster scope.
     constexpr bool kClu = CG == 2;
     const int tile_step = gridDim.x / CG;
     const int tile0 = blockIdx.x / CG;
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     const int m0 = tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
                     const int n0 = tn * BN + static_cast<int>(rank) * T::BN_CTA;
                     for (int kb = 0; kb < args.num_kb; ++kb) {
-                        if (!wait_bar<kClu>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
+                        if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                             ok = false;
                             break;
                         }
@@ -225,7 +228,13 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             for (int j = 0; j < T::NBOX; ++j)
                                 tma_load_2d(sB + stage * T::B_BYTES + j * (T::BK * 128), &tmB, fb, n0 + j * T::CW, k0);
                         } else {
-                            mbar_arrive_expect_tx_cluster(fb, T::STAGE_BYTES);
+                            // Only the leader arms the barrier, for both CTAs'
+                            // bytes; the peer's copies just complete on it. A
+                            // peer copy landing first drives the transaction
+                            // count negative, which the barrier allows, and the
+                            // leader's pending arrival keeps the phase open.
+                            if (leader)
+                                mbar_arrive_expect_tx(full_bar(stage), 2 * T::STAGE_BYTES);
                             tma_load_2d_pair(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
 #pragma unroll
                             for (int j = 0; j < T::NBOX; ++j)
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 // above, so no copy or commit is in flight when the CTA ends.
                 if (ok) {
                     for (int i = 0; i < T::STAGES; ++i) {
-                        if (!wait_bar<kClu>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer))
+                        if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer))
                             break;
                         if (++stage == T::STAGES) {
                             stage = 0;
@@ -348,14 +357,14 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
             for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {
+                if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {  // peer epilogue releases: cluster scope
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
                 for (int kb = 0; kb < args.num_kb; ++kb) {
-                    if (!wait_bar<kClu>(full_bar(stage), phase, wc, kErrTimeoutMma)) {
+                    if (!wait_bar<false>(full_bar(stage), phase, wc, kErrTimeoutMma)) {
                         ok = false;
                         break;
                     }
@@ -416,7 +425,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         const float alpha = args.alpha, beta = args.beta;
         const int64_t ldc = args.N;
         for (int t = tile0; t < args.num_tiles; t += tile_step) {
-            if (!wait_bar<kClu>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
+            if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
                 break;
             tc_fence_after();
             int tm, tn;

@@ -1,0 +1,130 @@
+"""On-device sweep of every candidate (tile, schedule) for GEMM shapes.
+
+For each shape and dtype, every configuration the kernels support (tile N,
+single SM or CTA pair, raster order, raster group) is timed the way the
+benchmark times the dispatcher's choice: L2 flushed by a 256 MiB write
+before each run, a CUDA event pair around each gemm_run, median of the
+timed runs. Results go to a JSON file; ``--table`` also writes the winners
+as the dispatcher's committed table (``csrc/sweep_table.inc``).
+
+This is the offline counterpart of the tactic ranking in the FlashInfer
+pull request "fix(fp4_gemm autotune) SM107 kernel family excluded from
+autotune candidates": measure every candidate instead of truncating a
+scored list, then freeze the winners so that the runtime does no tuning.
+
+  python -m shape_adaptive_tile_gb300.sweep --out sweep.json [--table] [--shapes tf32:2048x2048x2048 ...]
+"""
+from __future__ import annotations
+
+import argparse
+import itertools
+import json
+import os
+import statistics
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+TABLE = os.path.join(HERE, "csrc", "sweep_table.inc")
+DT_CODE = {"tf32": 0, "bf16": 1, "fp16": 2}
+
+
+def candidates(M, N, K, dtype, tma_ok):
+    out = []
+    for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
+        if not tma_ok and (cg == 2 or bn == 64):
+            continue
+        for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
+            out.append(f"{bn},{cg},{raster},{group}")
+    return out
+
+
+def time_config(sat, torch, M, N, K, dtype, config, dA, dB, dC, flush, runs, warmup):
+    stream = torch.cuda.current_stream()
+    with sat.Plan(M, N, K, dtype, config) as plan:
+        for _ in range(warmup):
+            plan.run(dA, dB, dC, 1.0, 0.0, stream.cuda_stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            plan.run(dA, dB, dC, 1.0, 0.0, stream.cuda_stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+        t = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+        return {"config": config, "plan": plan.describe(), "median_ms": statistics.median(t), "min_ms": t[0]}
+
+
+def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None):
+    es = 4 if dtype == "tf32" else 2
+    tma_ok = (K * es) % 16 == 0 and (N * es) % 16 == 0
+    rng = np.random.default_rng(0)
+    tdt = {"tf32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    dA = torch.from_numpy(rng.integers(-4, 5, (M, K)).astype(np.float32)).to("cuda", tdt)
+    dB = torch.from_numpy(rng.integers(-4, 5, (K, N)).astype(np.float32)).to("cuda", tdt)
+    dC = torch.empty(M, N, device="cuda")
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    res = []
+    for cfg in configs or candidates(M, N, K, dtype, tma_ok):
+        r = time_config(sat, torch, M, N, K, dtype, cfg, dA, dB, dC, flush, runs, warmup)
+        r["tflops"] = 2.0 * M * N * K / (r["median_ms"] * 1e-3) / 1e12
+        res.append(r)
+    with sat.Plan(M, N, K, dtype) as p:
+        chosen = p.describe()
+    return {"dtype": dtype, "M": M, "N": N, "K": K, "results": res, "dispatcher": chosen}
+
+
+def write_table(entries, path=TABLE):
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0}}.",
+             "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
+             "// (median of L2-flushed runs) of every candidate configuration."]
+    for e in entries:
+        best = min(e["results"], key=lambda r: r["median_ms"])
+        bn, cg, raster, group = best["config"].split(",")[:4]
+        lines.append(f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0}}}},"
+                     f"  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+    lines.append("{-1, 0, 0, 0, {256, 1, 0, 8, 0}},")
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", required=True)
+    ap.add_argument("--shapes", nargs="*", help="dtype:MxNxK (default: every benchmark workload)")
+    ap.add_argument("--configs", nargs="*", help="restrict to these configurations")
+    ap.add_argument("--runs", type=int, default=30)
+    ap.add_argument("--table", action="store_true", help="also write csrc/sweep_table.inc")
+    args = ap.parse_args(argv)
+    sys.path.insert(0, os.path.dirname(HERE))
+    import torch
+    import shape_adaptive_tile_gb300 as sat
+    import synth_inputs as si
+    torch.cuda.set_device(0)
+    sat.build()
+    if args.shapes:
+        shapes = []
+        for s in args.shapes:
+            dt, dims = s.split(":")
+            shapes.append((dt, tuple(int(x) for x in dims.split("x"))))
+    else:
+        shapes = sorted({(w[1], w[2]) for w in si.WORKLOADS})
+    entries = []
+    for dt, (M, N, K) in shapes:
+        e = sweep_shape(sat, torch, M, N, K, dt, args.runs, configs=args.configs)
+        best = min(e["results"], key=lambda r: r["median_ms"])
+        print(f"{dt} {M}x{N}x{K}: best {best['config']} {best['tflops']:.1f} TFLOP/s; "
+              f"dispatcher [{e['dispatcher']}]", flush=True)
+        for r in sorted(e["results"], key=lambda r: r["median_ms"])[:5]:
+            print(f"    {r['config']:>12} {r['median_ms'] * 1e3:9.1f} us {r['tflops']:8.1f} TFLOP/s", flush=True)
+        entries.append(e)
+        with open(args.out, "w") as f:
+            json.dump(entries, f, indent=1)
+    if args.table:
+        write_table(entries)
+
+
+if __name__ == "__main__":
+    main()
