@@ -64,13 +64,18 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
             return c;
         }
     }
-    // Analytic rule. Per-SM rates: dense tensor FLOP per clock (bf16/fp16
-    // 8192, tf32 4096) and a sustained operand-fill rate from L2 of about
-    // 64 bytes per clock per SM; the plain-load path fills far slower.
+    // Analytic rule, calibrated on the sweep: per-SM dense tensor rate
+    // (bf16/fp16 8192 FLOP per clock, tf32 4096), a sustained operand fill
+    // from L2 of about 64 bytes per clock per SM for TMA (the plain-load path
+    // fills far slower), about 22 bytes per clock of HBM bandwidth per SM
+    // (6.7 TB/s over 152 SMs at ~2 GHz), and a fixed cost per wave
+    // (prologue, pipeline fill, final epilogue).
     const double es = dt == 0 ? 4.0 : 2.0;
     const double flop_clk = dt == 0 ? 4096.0 : 8192.0;
     const double fill_clk = tma_ok ? 64.0 : 12.0;
-    const double epi_clk = 4096.0;  // epilogue not hidden behind the last tile
+    const double hbm_clk = 22.0 * sm_count;
+    const double wave_cost = 6000.0;
+    const double hbm = (es * (double)(M * K + K * N) + 8.0 * (double)(M * N)) / hbm_clk;
     struct Cand { int bn, cg; };
     const Cand cands[] = {{256, 2}, {128, 2}, {256, 1}, {128, 1}, {64, 1}};
     double best_t = 1e300;
@@ -78,6 +83,8 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     for (const Cand& cd : cands) {
         if (!tma_ok && (cd.cg == 2 || cd.bn == 64))
             continue;
+        if (cd.cg == 2 && M <= 128)
+            continue;  // a CTA pair would leave its second 128 rows empty
         const int64_t tm = 128 * cd.cg;
         const int64_t tiles = cdiv(M, tm) * cdiv(N, cd.bn);
         const int64_t slots = std::max<int64_t>(1, sm_count / cd.cg);
@@ -85,7 +92,7 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
         // Per CTA: its MMA share and the bytes it loads per unit of K.
         const double mma = 2.0 * 128.0 * cd.bn * K / flop_clk;
         const double fill = (128.0 + cd.bn / cd.cg) * es * K / fill_clk;
-        const double t = waves * std::max(mma, fill) + epi_clk;
+        const double t = std::max(waves * (std::max(mma, fill) + wave_cost), hbm);
         // Prefer the larger tile unless the smaller is clearly faster.
         if (t < best_t * 0.97) {
             best_t = t;
