@@ -98,7 +98,8 @@ struct gemm_plan {
     mutable std::mutex mu;
     mutable const void* map_A = nullptr;
     mutable const void* map_B = nullptr;
-    mutable CUtensorMap tmA{}, tmB{};
+    mutable const void* map_C = nullptr;
+    mutable CUtensorMap tmA{}, tmB{}, tmC{};
 };
 
 namespace {
@@ -308,7 +309,23 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     a.err = p->d_err;
     a.timeout_ns = p->timeout_ns;
 
-    CUtensorMap tmA{}, tmB{};
+    // C goes through the bulk-store epilogue when its base and row stride
+    // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
+    const bool c_tma = (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+    a.c_tma = c_tma ? 1 : 0;
+    CUtensorMap tmA{}, tmB{}, tmC{};
+    if (c_tma) {
+        std::lock_guard<std::mutex> lock(p->mu);
+        if (p->map_C != C) {
+            const int rc = encode_2d(&p->tmC, sat::kDtTF32, C, p->N, p->M, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc) {
+                p->map_C = nullptr;
+                return rc;
+            }
+            p->map_C = C;
+        }
+        tmC = p->tmC;
+    }
     if (use_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
         if (p->map_A != A) {
@@ -332,7 +349,7 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         tmA = p->tmA;
         tmB = p->tmB;
     }
-    e = k->launch(&tmA, &tmB, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
+    e = k->launch(&tmA, &tmB, &tmC, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
     return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the GEMM kernel");
 }
 

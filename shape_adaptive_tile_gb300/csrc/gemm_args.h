@@ -25,6 +25,7 @@ struct GemmArgs {
     int num_kb;                // ceil(K / BK)
     int group;                 // rasterisation group size (>= 1)
     int raster;                // 0: groups along M, 1: groups along N
+    int c_tma;                 // 1: C is written (and read) through the TMA store path
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;
 };

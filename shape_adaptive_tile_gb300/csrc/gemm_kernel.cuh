@@ -53,8 +53,12 @@ struct Traits {
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = NBOX * BK * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_FLOATS = 32 * 33;      // per epilogue warp
-    static constexpr int EPI_BYTES = 4 * EPI_FLOATS * 4;
+    // Epilogue staging, per warp: two 4 KB buffers (32 rows x 128 bytes, in
+    // the TMA store's 128-byte swizzle) for the bulk-store path; the
+    // row-store fallback uses the first 32 x 33 floats as a transpose buffer.
+    static constexpr int EPI_FLOATS = 32 * 33;
+    static constexpr int EPI_WARP_BYTES = 2 * 4096;
+    static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
@@ -135,7 +139,7 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
 template <int DT, int BN, int CG, int PROD>
 __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     sat_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs args)
+                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
     using T = Traits<DT, BN, CG, PROD>;
     extern __shared__ uint8_t smem_raw[];
@@ -181,6 +185,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (args.c_tma && warp == T::EPI_WARP0 && lane == 0)
+        tma_prefetch_desc(&tmC);
     if (warp == T::MMA_WARP) {
         tmem_alloc<CG>(smem_u32(tmem_slot), T::TMEM_COLS);
         tmem_relinquish<CG>();
@@ -418,10 +424,12 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int ew = warp - T::EPI_WARP0;      // 0..3
         const int sub = warp & 3;                // TMEM lane quarter this warp may access
-        float* const buf = epi + ew * T::EPI_FLOATS;
+        float* const buf = epi + ew * (T::EPI_WARP_BYTES / 4);
+        const uint32_t sbuf0 = smem_u32(buf);   // 1024-byte aligned
         const uint32_t tempty0 = CG == 2 ? map_to_cta(tempty_bar(0), 0) : tempty_bar(0);
         int acc = 0;
         uint32_t acc_phase = 0;
+        int chunk_ctr = 0;                       // alternates the two staging buffers
         const float alpha = args.alpha, beta = args.beta;
         const int64_t ldc = args.N;
         for (int t = tile0; t < args.num_tiles; t += tile_step) {
@@ -450,6 +458,54 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             mbar_arrive_cluster(tempty0 + 8u * acc);
                     }
                 }
+                if (args.c_tma) {
+                    // Bulk-store path: this thread owns row (row0 + lane) of the
+                    // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
+                    // (16-byte piece q of row l at position q ^ (l & 7): each
+                    // group of 8 lanes covers all 32 banks) and let one lane
+                    // hand the chunk to the TMA engine, which clips it to M x N.
+                    const int grow = row0 + lane;
+                    const int gcol0 = n0 + c * 32;
+                    float cv[32];
+                    if (beta != 0.0f) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            args.C + static_cast<int64_t>(grow) * ldc + gcol0);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (grow < args.M && gcol0 + 4 * q < args.N)
+                                x = src[q];
+                            cv[4 * q] = x.x;
+                            cv[4 * q + 1] = x.y;
+                            cv[4 * q + 2] = x.z;
+                            cv[4 * q + 3] = x.w;
+                        }
+                    }
+                    const uint32_t sb = sbuf0 + static_cast<uint32_t>(chunk_ctr & 1) * 4096u;
+                    if (lane == 0)
+                        bulk_wait_read<1>();  // the store that last read this buffer is done with it
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            v[e] = alpha * __uint_as_float(r[4 * q + e]);
+                            if (beta != 0.0f)
+                                v[e] = fmaf(beta, cv[4 * q + e], v[e]);
+                        }
+                        st_shared_v4(sb + static_cast<uint32_t>(lane * 128 + ((q ^ (lane & 7)) << 4)), v[0], v[1],
+                                     v[2], v[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < args.M && gcol0 < args.N) {
+                        tma_store_2d(&tmC, sb, gcol0, row0);
+                        bulk_commit();
+                    }
+                    ++chunk_ctr;
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     buf[lane * 33 + j] = __uint_as_float(r[j]);
@@ -472,6 +528,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             if (acc == 0)
                 acc_phase ^= 1u;
         }
+        if (args.c_tma && lane == 0)
+            bulk_wait<0>();  // every bulk store of this warp has completed
+        __syncwarp();
     }
 
     // ------------------------------------------------------------- teardown

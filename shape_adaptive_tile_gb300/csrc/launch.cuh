@@ -15,8 +15,8 @@ cudaError_t prepare_variant()
 }
 
 template <int DT, int BN, int CG, int PROD>
-cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs* args, int grid,
-                           cudaStream_t stream)
+cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
+                           const GemmArgs* args, int grid, cudaStream_t stream)
 {
     using T = Traits<DT, BN, CG, PROD>;
     cudaLaunchConfig_t cfg = {};
@@ -33,7 +33,7 @@ cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD>, *tmA, *tmB, *args);
+    return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD>, *tmA, *tmB, *tmC, *args);
 }
 
 template <int DT, int BN, int CG, int PROD>

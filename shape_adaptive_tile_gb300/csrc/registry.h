@@ -21,8 +21,8 @@ struct KernelEntry {
     int b_swizzle; // CUtensorMapSwizzle of B's tensor map
     cudaError_t (*prepare)();  // sets the kernel's dynamic shared-memory limit
     int (*max_clusters)();     // co-resident CTA pairs on this device (cg == 2), 0 if unknown
-    cudaError_t (*launch)(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs* args, int grid,
-                          cudaStream_t stream);
+    cudaError_t (*launch)(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
+                          const GemmArgs* args, int grid, cudaStream_t stream);
 };
 
 // Defined in kernels_<dtype>.cu.

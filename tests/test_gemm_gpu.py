@@ -103,6 +103,21 @@ def test_misaligned_pointers_take_the_plain_path(dtype):
     checks.assert_bit_exact(dC.cpu().numpy(), ref32, "misaligned")
 
 
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_c_not_16_byte_aligned_takes_the_row_store_epilogue(dtype):
+    """C one float past a 16-byte boundary rules out the bulk (TMA) store;
+    the row-store epilogue must give the same bits, beta term included."""
+    M, N, K = 200, 256, 64
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 15, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, dtype)
+    flatC = to_dev(np.concatenate([np.zeros(1, np.float32), C0.ravel()]))
+    with sat.Plan(M, N, K, dtype) as plan:
+        run(plan, to_dev(A, dtype), to_dev(B, dtype), flatC.data_ptr() + 4, 1.5, -0.5)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    checks.assert_bit_exact(flatC[1:].view(M, N).cpu().numpy(), ref32, "C misaligned")
+
+
 def test_error_codes():
     with pytest.raises(sat.GemmError):
         sat.gemm_plan_create(-1, 4, 4, "tf32")
