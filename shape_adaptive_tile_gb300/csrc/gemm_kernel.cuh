@@ -53,12 +53,13 @@ struct Traits {
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = NBOX * BK * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // Epilogue staging, per warp: two 4 KB buffers (32 rows x 128 bytes, in
-    // the TMA store's 128-byte swizzle) for the bulk-store path; the
-    // row-store fallback uses the first 32 x 33 floats as a transpose buffer.
-    static constexpr int EPI_FLOATS = 32 * 33;
-    static constexpr int EPI_WARP_BYTES = 2 * 4096;
-    static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+    // Epilogue: 8 warps (4 with the plain-load producer), two (one) per TMEM
+    // lane quarter, taking alternate 32-column chunks. Each has one 4 KB staging buffer: 32 rows x 128
+    // bytes in the TMA store's 128-byte swizzle for the bulk-store path, or
+    // a 32 x 32 XOR-swizzled transpose buffer for the row-store fallback.
+    static constexpr int EPI_WARPS = PROD == kProdTMA ? 8 : 4;   // plain-load CTAs keep 9 warps
+    static constexpr int EPI_WARP_BYTES = 4096;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
@@ -66,7 +67,7 @@ struct Traits {
     static constexpr int NPW = PROD == kProdTMA ? 1 : 4;   // producer warps
     static constexpr int MMA_WARP = NPW;
     static constexpr int EPI_WARP0 = NPW + 1;
-    static constexpr int THREADS = (NPW + 1 + 4) * 32;
+    static constexpr int THREADS = (NPW + 1 + EPI_WARPS) * 32;
     static constexpr int ACC_COLS = BN;             // fp32 accumulator: one column per element
     static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     static constexpr uint32_t FMT = DT == kDtTF32 ? kFmtTF32 : DT == kDtBF16 ? kFmtBF16 : kFmtF16;
@@ -162,8 +163,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * T::STAGES + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * T::STAGES + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * T::STAGES + 4);
-    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 8 * (2 * T::STAGES + 5));
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 8 * (2 * T::STAGES + 5) + 4);
+    const uint32_t tmem_ready_bar = bars + 8u * (2 * T::STAGES + 5);   // pair: the peer's TMEM is allocated
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 8 * (2 * T::STAGES + 6));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 8 * (2 * T::STAGES + 6) + 4);
 
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
@@ -175,9 +177,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4 * CG);
+            mbar_init(tempty_bar(a), T::EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(tmem_ready_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -187,16 +190,27 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     }
     if (args.c_tma && warp == T::EPI_WARP0 && lane == 0)
         tma_prefetch_desc(&tmC);
-    if (warp == T::MMA_WARP) {
-        tmem_alloc<CG>(smem_u32(tmem_slot), T::TMEM_COLS);
-        tmem_relinquish<CG>();
-    }
-    tc_fence_before();
+    // Barrier initialisation is published to the CTA (and, for a pair, to
+    // the peer); the producer then starts at once. Tensor memory is
+    // allocated meanwhile and published only to the MMA and epilogue warps
+    // (named barrier 1); in a pair the peer also tells the leader, whose MMAs
+    // write the peer's tensor memory, through tmem_ready_bar.
     __syncthreads();
     if constexpr (CG == 2)
         cluster_sync();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    uint32_t tmem_base = 0;
+    if (warp >= T::MMA_WARP) {
+        if (warp == T::MMA_WARP) {
+            tmem_alloc<CG>(smem_u32(tmem_slot), T::TMEM_COLS);
+            tmem_relinquish<CG>();
+        }
+        tc_fence_before();
+        named_bar_sync(1, (1 + T::EPI_WARPS) * 32);
+        tc_fence_after();
+        tmem_base = *tmem_slot;
+        if (CG == 2 && !leader && warp == T::MMA_WARP && lane == 0)
+            mbar_arrive_cluster(map_to_cta(tmem_ready_bar, 0));
+    }
 
     const WaitCtl wc{abort_flag, args.err, args.timeout_ns};
     // Barriers completed by TMA transactions or tcgen05.commit need only
@@ -362,6 +376,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
+            if constexpr (CG == 2)
+                ok = wait_bar<true>(tmem_ready_bar, 0, wc, kErrTimeoutMma);
             for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
                 if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {  // peer epilogue releases: cluster scope
                     ok = false;
@@ -422,16 +438,18 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - T::EPI_WARP0;      // 0..3
+        const int ew = warp - T::EPI_WARP0;      // 0..7
         const int sub = warp & 3;                // TMEM lane quarter this warp may access
+        constexpr int CSTEP = T::EPI_WARPS / 4;  // warps per TMEM lane quarter
+        const int half = ew >> 2;                // this warp takes chunks half, half + CSTEP, ...
         float* const buf = epi + ew * (T::EPI_WARP_BYTES / 4);
-        const uint32_t sbuf0 = smem_u32(buf);   // 1024-byte aligned
+        const uint32_t sb = smem_u32(buf);       // 1024-byte aligned
         const uint32_t tempty0 = CG == 2 ? map_to_cta(tempty_bar(0), 0) : tempty_bar(0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        int chunk_ctr = 0;                       // alternates the two staging buffers
         const float alpha = args.alpha, beta = args.beta;
         const int64_t ldc = args.N;
+        constexpr int NCHUNK = BN / 32;
         for (int t = tile0; t < args.num_tiles; t += tile_step) {
             if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
                 break;
@@ -443,12 +461,12 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
                                    static_cast<uint32_t>(acc * T::ACC_COLS);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = half; c < NCHUNK; c += CSTEP) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, r);
                 tmem_wait_ld();
-                if (c == BN / 32 - 1) {
-                    // All TMEM reads of this accumulator are done: hand it back.
+                if (c + CSTEP >= NCHUNK) {
+                    // This warp's TMEM reads of the accumulator are done: hand it back.
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -458,6 +476,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             mbar_arrive_cluster(tempty0 + 8u * acc);
                     }
                 }
+                const int gcol0 = n0 + c * 32;
                 if (args.c_tma) {
                     // Bulk-store path: this thread owns row (row0 + lane) of the
                     // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
@@ -465,7 +484,6 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     // group of 8 lanes covers all 32 banks) and let one lane
                     // hand the chunk to the TMA engine, which clips it to M x N.
                     const int grow = row0 + lane;
-                    const int gcol0 = n0 + c * 32;
                     float cv[32];
                     if (beta != 0.0f) {
                         const float4* src = reinterpret_cast<const float4*>(
@@ -481,9 +499,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             cv[4 * q + 3] = x.w;
                         }
                     }
-                    const uint32_t sb = sbuf0 + static_cast<uint32_t>(chunk_ctr & 1) * 4096u;
                     if (lane == 0)
-                        bulk_wait_read<1>();  // the store that last read this buffer is done with it
+                        bulk_wait_read<0>();  // the previous store has finished reading the buffer
                     __syncwarp();
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -503,20 +520,23 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         tma_store_2d(&tmC, sb, gcol0, row0);
                         bulk_commit();
                     }
-                    ++chunk_ctr;
                     continue;
                 }
+                // Row-store fallback: transpose through the XOR-swizzled
+                // buffer (element (row l, column j) at l*32 + (j ^ l): conflict
+                // free both ways), then each row is written by the warp as 32
+                // consecutive floats, masked to M x N.
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    buf[lane * 33 + j] = __uint_as_float(r[j]);
+                    buf[lane * 32 + (j ^ lane)] = __uint_as_float(r[j]);
                 __syncwarp();
-                const int col = n0 + c * 32 + lane;
+                const int col = gcol0 + lane;
                 if (col < args.N) {
                     float* cp = args.C + static_cast<int64_t>(row0) * ldc + col;
                     const int rows = min(32, args.M - row0);
 #pragma unroll 4
                     for (int i = 0; i < rows; ++i) {
-                        float v = alpha * buf[i * 33 + lane];
+                        float v = alpha * buf[i * 32 + (lane ^ i)];
                         if (beta != 0.0f)
                             v = fmaf(beta, cp[i * ldc], v);
                         cp[i * ldc] = v;
