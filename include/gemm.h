@@ -55,18 +55,23 @@ typedef struct gemm_plan gemm_plan; /* opaque */
  * Choose the kernel (tile shape, CTA-pair or single SM, stage count, raster
  * order, load path) for this problem on the CURRENT device, and prepare it.
  * M, N, K >= 0 and each < 2^31. Allocates host state and one 4-byte device
- * error word, both owned by the plan. Returns NULL on failure; the reason is
- * in gemm_last_error(). Must not be called during CUDA stream capture.
+ * error word, both owned by the plan, and, when the choice splits K, a device
+ * workspace of splits x ceil(M/256)*256 x N floats for the partial tiles.
+ * Returns NULL on failure; the reason is in gemm_last_error(). Must not be
+ * called during CUDA stream capture.
  */
 gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype);
 
 /*
  * As gemm_plan_create, but with the dispatcher's choice replaced by
- * `config` = "bn,cg,raster,group" (bn in {64,128,256}; cg 1 or 2, where 2
- * needs bn >= 128; raster 0 = groups along M, 1 = along N; group >= 1),
- * optionally followed by ",plain" to force the plain-load producer. NULL or
- * "" means the dispatcher decides. For sweeps and tests; the result is the
- * same GEMM whatever the configuration.
+ * `config` = "bn,cg,raster,group[,splits]" (bn in {64,128,256}; cg 1 or 2,
+ * where 2 needs bn >= 128; raster 0 = groups along M, 1 = along N;
+ * group >= 1; splits 1..16 K splits, default 1), optionally followed by
+ * ",plain" to force the plain-load producer. NULL or "" means the dispatcher
+ * decides. For sweeps and tests; every configuration computes the same GEMM
+ * (with splits > 1 the K sum is split into fixed slices whose partial tiles
+ * are added in fixed order, so the bits can differ from splits = 1 but are
+ * identical from run to run).
  */
 gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config);
 
@@ -81,8 +86,12 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
  * A and B must be aligned to their element size, C to 4 bytes
  * (GEMM_ERR_ALIGN otherwise); 16-byte aligned A/B with 16-byte-multiple row
  * strides take the TMA load path, anything else the plain-load path, with
- * identical results. The plan is read-only here, so one plan may run on
- * several streams or threads at once. Launch failures return
+ * identical results. A plan that splits K launches a second kernel on the
+ * same stream that sums the partial tiles in fixed order and applies alpha
+ * and beta; its workspace is then in use until that kernel ends, so runs of
+ * such a plan on different streams must be ordered by the caller. Other
+ * plans are read-only here and may run on several streams or threads at
+ * once. Launch failures return
  * GEMM_ERR_LAUNCH; kernel-side bounded-wait timeouts are reported by
  * gemm_plan_status().
  */
@@ -132,7 +141,7 @@ int gemm_selftest_bounded_wait(uint64_t timeout_ns);
  * Host-only view of the dispatcher (no device is touched): the choice that
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
- * strides are multiples of 16 bytes). Writes "bn,cg,raster,group,source"
+ * strides are multiples of 16 bytes). Writes "bn,cg,raster,group,splits,source"
  * (source: rule or table) into `out` (NUL-terminated, at most `out_len`
  * bytes). Returns 0, or GEMM_ERR_ARG on bad arguments.
  */

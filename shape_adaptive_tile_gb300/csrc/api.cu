@@ -93,6 +93,12 @@ struct gemm_plan {
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
     int grid_tma = 0, grid_plain = 0;
     uint32_t* d_err = nullptr;
+    // Split-K: `splits` slices of `ws_rows` x N floats in `ws`, reduced in
+    // fixed order into C; tmW describes ws for the bulk-store epilogue.
+    int splits = 1, kb_per_split = 0, ws_rows = 0;
+    float* ws = nullptr;
+    bool ws_tma = false;
+    CUtensorMap tmW{};
     unsigned long long timeout_ns = 2000000000ull;
     char desc[256] = "";
     mutable std::mutex mu;
@@ -107,7 +113,7 @@ namespace {
 int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
 {
     const int64_t tm = 128 * e->cg;
-    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn);
+    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn) * p->splits;
     int64_t slots = p->sm_count / e->cg;
     if (e->cg == 2) {
         // Not every SM need be able to pair with a neighbour: ask the
@@ -209,16 +215,38 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             return nullptr;
         }
     }
+    // Split-K over this plan's tiles (TMA and plain-load variants share the
+    // tile N, and both use single-CTA row tiles of 128 when plain).
+    const int bk = (p->tma ? p->tma : p->plain)->bk;
+    const int64_t num_kb = (K + bk - 1) / bk;
+    p->splits = c.splits > 1 && num_kb > 1 ? c.splits : 1;
+    if (p->splits > num_kb)
+        p->splits = static_cast<int>(num_kb);
+    p->kb_per_split = static_cast<int>((num_kb + p->splits - 1) / p->splits);
+    if (p->splits > 1)  // no empty split
+        p->splits = static_cast<int>((num_kb + p->kb_per_split - 1) / p->kb_per_split);
     if (p->tma)
         p->grid_tma = grid_for(p, p->tma);
     p->grid_plain = grid_for(p, p->plain);
     e = cudaMalloc(&p->d_err, sizeof(uint32_t));
     if (e == cudaSuccess)
         e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
+    if (e == cudaSuccess && p->splits > 1) {
+        p->ws_rows = static_cast<int>((M + 255) / 256 * 256);
+        const size_t bytes = static_cast<size_t>(p->splits) * p->ws_rows * static_cast<size_t>(N) * sizeof(float);
+        e = cudaMalloc(&p->ws, bytes);
+        if (e == cudaSuccess && (N * 4) % 16 == 0) {
+            if (encode_2d(&p->tmW, sat::kDtTF32, p->ws, N, static_cast<uint64_t>(p->splits) * p->ws_rows, 32u, 32u,
+                          CU_TENSOR_MAP_SWIZZLE_128B) == 0)
+                p->ws_tma = true;
+        }
+    }
     if (e != cudaSuccess) {
-        cuda_fail(e, "allocating the device error word");
+        cuda_fail(e, "allocating the device error word and workspace");
         if (p->d_err)
             cudaFree(p->d_err);
+        if (p->ws)
+            cudaFree(p->ws);
         delete p;
         return nullptr;
     }
@@ -228,9 +256,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
     const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
-    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d grid%d %s",
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
-                  p->tma ? "tma" : "plain", c.raster, c.group, p->tma ? p->grid_tma : p->grid_plain, source);
+                  p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
+                  source);
     return p;
 }
 
@@ -254,6 +283,8 @@ void gemm_plan_destroy(gemm_plan* plan)
         return;
     if (plan->d_err)
         cudaFree(plan->d_err);
+    if (plan->ws)
+        cudaFree(plan->ws);
     delete plan;
 }
 
@@ -302,8 +333,20 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     a.beta = beta;
     a.tiles_m = static_cast<int>((p->M + 128 * k->cg - 1) / (128 * k->cg));
     a.tiles_n = static_cast<int>((p->N + k->bn - 1) / k->bn);
-    a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = static_cast<int>((p->K + k->bk - 1) / k->bk);
+    a.splits = p->splits;
+    a.kb_per_split = p->splits > 1 ? p->kb_per_split : a.num_kb;
+    a.num_tiles = a.tiles_m * a.tiles_n * a.splits;
+    a.out_rows = static_cast<int>(p->M);
+    const bool split = p->splits > 1;
+    if (split) {
+        // The GEMM writes raw fp32 partial tiles to the workspace; the
+        // reduction applies alpha and beta.
+        a.C = p->ws;
+        a.alpha = 1.0f;
+        a.beta = 0.0f;
+        a.out_rows = p->ws_rows;
+    }
     a.group = p->choice.group;
     a.raster = p->choice.raster;
     a.err = p->d_err;
@@ -311,10 +354,12 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
 
     // C goes through the bulk-store epilogue when its base and row stride
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
-    const bool c_tma = (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+    const bool c_tma = split ? p->ws_tma : (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     CUtensorMap tmA{}, tmB{}, tmC{};
-    if (c_tma) {
+    if (split && c_tma) {
+        tmC = p->tmW;
+    } else if (c_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
         if (p->map_C != C) {
             const int rc = encode_2d(&p->tmC, sat::kDtTF32, C, p->N, p->M, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -350,7 +395,15 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         tmB = p->tmB;
     }
     e = k->launch(&tmA, &tmB, &tmC, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
-    return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the GEMM kernel");
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the GEMM kernel");
+    if (split) {
+        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C,
+                                      static_cast<long long>(p->M * p->N), alpha, beta, p->sm_count, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launching the split-K reduction");
+    }
+    return GEMM_OK;
 }
 
 int gemm_run_host(const gemm_plan* p, const void* hA, const void* hB, float* hC, float alpha, float beta, void* dA,
@@ -431,8 +484,8 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
         return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
     const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
-    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
-                  c.source == 1 ? "table" : "rule");
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.splits > 1 ? c.splits : 1, c.source == 1 ? "table" : "rule");
     return GEMM_OK;
 }
 

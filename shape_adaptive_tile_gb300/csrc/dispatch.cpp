@@ -43,10 +43,14 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool parse_choice(const char* spec, Choice* out)
 {
     Choice c{};
-    if (!spec || std::sscanf(spec, "%d,%d,%d,%d", &c.bn, &c.cg, &c.raster, &c.group) != 4)
+    c.splits = 1;
+    if (!spec)
+        return false;
+    const int n = std::sscanf(spec, "%d,%d,%d,%d,%d", &c.bn, &c.cg, &c.raster, &c.group, &c.splits);
+    if (n != 4 && n != 5)
         return false;
     if ((c.bn != 64 && c.bn != 128 && c.bn != 256) || (c.cg != 1 && c.cg != 2) || (c.raster != 0 && c.raster != 1) ||
-        c.group < 1 || (c.cg == 2 && c.bn == 64))
+        c.group < 1 || (c.cg == 2 && c.bn == 64) || c.splits < 1 || c.splits > 16)
         return false;
     c.source = 2;
     *out = c;
@@ -59,6 +63,8 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
         if (r.dt == dt && r.M == M && r.N == N && r.K == K && (tma_ok || r.c.cg == 1)) {
             Choice c = r.c;
             c.source = 1;
+            if (c.splits < 1)
+                c.splits = 1;
             if (!tma_ok && c.bn == 64)
                 c.bn = 128;
             return c;
@@ -103,6 +109,26 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     best.raster = 0;
     best.group = best.cg == 2 ? 4 : 8;
     best.source = 0;
+    best.splits = 1;
+    // Split K when the chosen tiles would leave most SMs idle and K is long:
+    // each split needs at least 16 k-blocks, and the fixed-order reduction
+    // (S + 2 floats of traffic per output) plus its launch must pay off.
+    {
+        const int64_t tm = 128 * best.cg;
+        const int64_t ctas = cdiv(M, tm) * cdiv(N, best.bn) * best.cg;
+        const int64_t kb = cdiv(K, dt == 0 ? 32 : 64);
+        int s = 1;
+        while (s < 8 && ctas * s * 2 <= sm_count && kb / (s * 2) >= 16)
+            s *= 2;
+        if (s > 1) {
+            const double mma = 2.0 * 128.0 * best.bn * K / flop_clk;
+            const double fill = (128.0 + best.bn / best.cg) * es * K / fill_clk;
+            const double t1 = std::max(mma, fill) + wave_cost;
+            const double ts = std::max(mma, fill) / s + wave_cost + 6000.0 + (s + 2.0) * 4.0 * (double)(M * N) / hbm_clk;
+            if (ts < 0.8 * t1)
+                best.splits = s;
+        }
+    }
     return best;
 }
 

@@ -10,14 +10,15 @@ struct Choice {
     int cg;       // 1 or 2 (CTA pair)
     int raster;   // 0: groups along M, 1: groups along N
     int group;    // raster group size in tiles
-    int source;   // 0: analytic rule, 1: committed sweep table
+    int source;   // 0: analytic rule, 1: committed sweep table, 2: forced
+    int splits;   // K splits (fixed-order reduction through a workspace); 0 or 1: none
 };
 
 // Picks tile and schedule. `tma_ok` says whether the TMA load path can be
 // used (16-byte-multiple row strides); when false only 1-SM tiles exist.
 Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool tma_ok);
 
-// Override for sweeps and tests: "bn,cg,raster,group" (e.g. "256,2,0,8").
+// Override for sweeps and tests: "bn,cg,raster,group[,splits]" (e.g. "256,2,0,8").
 // Returns false if `spec` is malformed.
 bool parse_choice(const char* spec, Choice* out);
 

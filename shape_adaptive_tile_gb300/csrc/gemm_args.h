@@ -18,11 +18,14 @@ struct GemmArgs {
     int M, N, K;
     const void* A;             // M x K row-major (plain-load producer only)
     const void* B;             // K x N row-major (plain-load producer only)
-    float* C;                  // M x N row-major
+    float* C;                  // output: C (M x N), or the split-K workspace (splits x out_rows x N)
     float alpha, beta;
     int tiles_m, tiles_n;      // tiles of (128 * cta_group) x BN
-    int num_tiles;
+    int num_tiles;             // work units: tiles_m * tiles_n * splits
     int num_kb;                // ceil(K / BK)
+    int splits;                // K splits (1: C is written directly)
+    int kb_per_split;          // k-blocks per split
+    int out_rows;              // rows of one split's slice of the output (M, or the workspace's padded M)
     int group;                 // rasterisation group size (>= 1)
     int raster;                // 0: groups along M, 1: groups along N
     int c_tma;                 // 1: C is written (and read) through the TMA store path

@@ -125,6 +125,24 @@ __device__ __forceinline__ uint32_t swz_kmajor(int r, int k)
     return static_cast<uint32_t>(r) * 128u + ((((kb >> 4) ^ static_cast<uint32_t>(r & 7)) << 4) | (kb & 15u));
 }
 
+// A work unit: output tile (tm, tn) of K split s, k-blocks [kb0, kb1).
+// Units of one split are consecutive, so CTAs running at the same time
+// share that split's K slice of the operands in L2.
+struct Unit {
+    int tm, tn, s, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
+{
+    Unit w;
+    const int per = a.tiles_m * a.tiles_n;
+    w.s = u / per;
+    tile_coord(u - w.s * per, a, w.tm, w.tn);
+    w.kb0 = w.s * a.kb_per_split;
+    w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
+    return w;
+}
+
 // Byte offset of B element (k, n) in the MN-major tile: column blocks of
 // 128 bytes, each BK rows of 128 bytes with the same XOR swizzle.
 template <int ES, int BK>
@@ -230,11 +248,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 // The pair's loads all complete on the leader's barrier.
                 const uint32_t full0 = CG == 2 ? map_to_cta(full_bar(0), 0) : full_bar(0);
                 for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                    int tm, tn;
-                    tile_coord(t, args, tm, tn);
-                    const int m0 = tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
-                    const int n0 = tn * BN + static_cast<int>(rank) * T::BN_CTA;
-                    for (int kb = 0; kb < args.num_kb; ++kb) {
+                    const Unit w = unit_coord(t, args);
+                    const int m0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
+                    const int n0 = w.tn * BN + static_cast<int>(rank) * T::BN_CTA;
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                             ok = false;
                             break;
@@ -292,11 +309,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                int tm, tn;
-                tile_coord(t, args, tm, tn);
-                const int m0 = tm * T::BM;
-                const int n0 = tn * BN;
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                const Unit w = unit_coord(t, args);
+                const int m0 = w.tm * T::BM;
+                const int n0 = w.tn * BN;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                         ok = false;
                         break;
@@ -385,7 +401,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                const Unit w = unit_coord(t, args);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar<false>(full_bar(stage), phase, wc, kErrTimeoutMma)) {
                         ok = false;
                         break;
@@ -397,7 +414,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     for (int ks = 0; ks < T::KSTEPS; ++ks) {
                         const uint64_t ad = sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
                         const uint64_t bd = sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
-                        mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                        mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb != w.kb0 || ks != 0) ? 1u : 0u);
                     }
                     issued = true;
                     if constexpr (CG == 1)
@@ -454,10 +471,11 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
                 break;
             tc_fence_after();
-            int tm, tn;
-            tile_coord(t, args, tm, tn);
-            const int row0 = tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
-            const int n0 = tn * BN;
+            const Unit w = unit_coord(t, args);
+            const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
+            const int n0 = w.tn * BN;
+            // Split s writes its slice of the output: rows s * out_rows + row.
+            const int yoff = w.s * args.out_rows;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
                                    static_cast<uint32_t>(acc * T::ACC_COLS);
 #pragma unroll 1
@@ -487,7 +505,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     float cv[32];
                     if (beta != 0.0f) {
                         const float4* src = reinterpret_cast<const float4*>(
-                            args.C + static_cast<int64_t>(grow) * ldc + gcol0);
+                            args.C + static_cast<int64_t>(grow) * ldc + gcol0);  // beta != 0 only unsplit
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -517,7 +535,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && row0 < args.M && gcol0 < args.N) {
-                        tma_store_2d(&tmC, sb, gcol0, row0);
+                        tma_store_2d(&tmC, sb, gcol0, yoff + row0);
                         bulk_commit();
                     }
                     continue;
@@ -532,7 +550,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 __syncwarp();
                 const int col = gcol0 + lane;
                 if (col < args.N) {
-                    float* cp = args.C + static_cast<int64_t>(row0) * ldc + col;
+                    float* cp = args.C + (static_cast<int64_t>(yoff) + row0) * ldc + col;
                     const int rows = min(32, args.M - row0);
 #pragma unroll 4
                     for (int i = 0; i < rows; ++i) {

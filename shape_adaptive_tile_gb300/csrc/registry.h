@@ -39,5 +39,7 @@ const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
 // Defined in aux_kernels.cu.
 cudaError_t launch_scale(float* C, long long n, float beta, cudaStream_t stream);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long n, float alpha,
+                                 float beta, int sm_count, cudaStream_t stream);
 
 }  // namespace sat

@@ -30,13 +30,20 @@ TABLE = os.path.join(HERE, "csrc", "sweep_table.inc")
 DT_CODE = {"tf32": 0, "bf16": 1, "fp16": 2}
 
 
-def candidates(M, N, K, dtype, tma_ok):
+def candidates(M, N, K, dtype, tma_ok, sm_count=152):
     out = []
+    kb = -(-K // (32 if dtype == "tf32" else 64))
     for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
         if not tma_ok and (cg == 2 or bn == 64):
             continue
         for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
             out.append(f"{bn},{cg},{raster},{group}")
+        # K splits only where the tiles alone leave at least half the SMs idle
+        ctas = -(-M // (128 * cg)) * -(-N // bn) * cg
+        for s in (2, 4, 8):
+            if ctas * s <= 2 * sm_count and kb // s >= 4:
+                for group in (2, 8):
+                    out.append(f"{bn},{cg},0,{group},{s}")
     return out
 
 
@@ -77,13 +84,15 @@ def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None):
 
 
 def write_table(entries, path=TABLE):
-    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0}}.",
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits}}.",
              "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
              "// (median of L2-flushed runs) of every candidate configuration."]
     for e in entries:
         best = min(e["results"], key=lambda r: r["median_ms"])
-        bn, cg, raster, group = best["config"].split(",")[:4]
-        lines.append(f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0}}}},"
+        parts = best["config"].split(",")
+        bn, cg, raster, group = parts[:4]
+        splits = parts[4] if len(parts) > 4 and parts[4] != "plain" else "1"
+        lines.append(f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}}}}},"
                      f"  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
     lines.append("{-1, 0, 0, 0, {256, 1, 0, 8, 0}},")
     with open(path, "w") as f:

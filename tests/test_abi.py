@@ -54,8 +54,8 @@ def test_plan_create_fails_cleanly_without_a_gpu(lib):
 
 
 def _choice(M, N, K, dt, sms=152, tma=True):
-    bn, cg, raster, group, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
-    return int(bn), int(cg), int(raster), int(group), source
+    bn, cg, raster, group, splits, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
+    return int(bn), int(cg), int(raster), int(group), int(splits), source
 
 
 @pytest.mark.parametrize("dt", ["tf32", "bf16", "fp16"])
@@ -63,8 +63,9 @@ def test_dispatcher_choices_are_compiled_variants(dt):
     for M, N, K in [(256, 256, 256), (2048, 2048, 2048), (8192, 8192, 8192), (768, 768, 768),
                     (8191, 4097, 2049), (16384, 1024, 4096), (128, 8192, 8192), (4096, 4096, 512), (1, 1, 1)]:
         for tma in (True, False):
-            bn, cg, raster, group, _ = _choice(M, N, K, dt, tma=tma)
+            bn, cg, raster, group, splits, _ = _choice(M, N, K, dt, tma=tma)
             assert bn in (64, 128, 256) and cg in (1, 2) and raster in (0, 1) and group >= 1
+            assert 1 <= splits <= 16
             if not tma:
                 assert cg == 1 and bn in (128, 256)   # plain-load producer exists only for these
 
@@ -73,9 +74,16 @@ def test_dispatcher_fills_the_machine_for_skinny_m():
     # 128 x 8192: one 128x256 tile per SM would occupy 32 of 152 SMs; the
     # choice must engage at least half of them.
     for dt in ("tf32", "bf16"):
-        bn, cg, *_ = _choice(128, 8192, 8192, dt)
-        tiles = -(-128 // (128 * cg)) * -(-8192 // bn)
+        bn, cg, _, _, splits, _ = _choice(128, 8192, 8192, dt)
+        tiles = -(-128 // (128 * cg)) * -(-8192 // bn) * splits
         assert min(tiles * cg, 152) >= 76
+
+
+def test_dispatcher_splits_k_only_when_tiles_leave_sms_idle():
+    # A long K over few tiles: the rule splits K; a large square problem never.
+    assert _choice(256, 256, 16384, "bf16")[4] > 1
+    assert _choice(4096, 4096, 4096, "bf16")[4] == 1
+    assert _choice(8192, 8192, 8192, "tf32")[4] == 1
 
 
 def test_dispatcher_rejects_bad_arguments():

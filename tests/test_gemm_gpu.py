@@ -20,9 +20,10 @@ from tests.gpu_util import run, run_np, stream, to_dev
 pytestmark = pytest.mark.gpu
 
 DTYPES = ["tf32", "bf16", "fp16"]
-# bn, cg, raster, group[, plain]
+# bn, cg, raster, group[, splits][, plain]
 CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,2,1,1",
-           "256,1,0,8,plain", "128,1,1,3,plain"]
+           "256,1,0,8,plain", "128,1,1,3,plain",
+           "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain"]
 SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
 
 
