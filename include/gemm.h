@@ -109,6 +109,42 @@ int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, floa
 int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* hC, float alpha, float beta,
                   void* dA, void* dB, float* dC, void* cuda_stream);
 
+/*
+ * Allocation-free GEMM. The pages have no counterpart to this entry point; it
+ * exists for callers that must not allocate device or host memory while they
+ * run: a framework that has reserved the device memory for its own pool, a
+ * latency-bound loop that cannot afford cudaFree's device synchronisation,
+ * or a host program that forbids device allocation after start-up.
+ * gemm_plan_create allocates (host state, an error word, a split-K
+ * workspace), so such callers use this instead.
+ *
+ * Computes the same C = alpha * A * B + beta * C as gemm_run, with the same
+ * arguments, conventions, alignment rules and the dispatcher's choice of
+ * kernel, but makes no plan and calls no cudaMalloc, cudaFree or other
+ * allocating routine. The kernel's scratch memory (a status word and, when K
+ * is split, the partial tiles) is one fixed 16 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *   - A problem whose split-K partial tiles need more than that array holds
+ *     (splits x M rounded up to the tile height x N floats > 16 MiB - 256
+ *     bytes; e.g. bf16 128 x 19456 x 8192, split 2 ways) is rejected with
+ *     GEMM_ERR_ARG and a message saying so; gemm_run serves it.
+ *   - The first call on each device looks up the array's address on that
+ *     device (so the device must be current); make that first call before
+ *     any CUDA stream capture.
+ *   - Every call shares the array, which keeps the previous call's contents;
+ *     the status word is cleared on the stream at the start of each call.
+ *     Calls whose kernels overlap on the GPU (different streams, or the same
+ *     stream from several threads without ordering) race on the array and may
+ *     produce wrong results: order them.
+ *   - A bounded wait that gives up inside the kernel still ends it; this
+ *     entry point has no status query (plans have gemm_plan_status).
+ * Returns 0 after enqueueing on `cuda_stream`, or a negative gemm_status_t
+ * with the reason in gemm_last_error().
+ */
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const void* A, const void* B, float* C,
+                     float alpha, float beta, void* cuda_stream);
+
 /* Free the plan and its device error word. NULL is accepted. Synchronises
  * nothing: do not destroy a plan whose runs may still be executing. */
 void gemm_plan_destroy(gemm_plan* plan);

@@ -82,6 +82,13 @@ int cuda_fail(cudaError_t e, const char* what)
 
 }  // namespace
 
+namespace sat {
+void set_last_error(const char* msg)
+{
+    std::snprintf(g_err, sizeof g_err, "%s", msg);
+}
+}  // namespace sat
+
 struct gemm_plan {
     int64_t M = 0, N = 0, K = 0;
     int dt = 0;

@@ -33,6 +33,9 @@ extern const int kNumEntriesBF16;
 extern const KernelEntry kEntriesFP16[];
 extern const int kNumEntriesFP16;
 
+// Sets the message gemm_last_error() returns on this thread (api.cu).
+void set_last_error(const char* msg);
+
 // Finds the variant, or nullptr.
 const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
 

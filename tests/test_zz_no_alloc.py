@@ -1,0 +1,103 @@
+"""gemm_run_noalloc, the allocation-free entry point, through the C ABI.
+
+It serves callers that must not allocate device memory while they run (a
+framework that owns the device memory, a latency-bound loop that cannot
+afford cudaFree's synchronisation, a host that forbids allocation after
+start-up). It must give exactly what a plan and gemm_run give for the same
+problem, and it must do so on two calls in a row: every call shares the
+library's fixed scratch array, so the second call must not be disturbed by
+what the first left there (its status word, its split-K partial tiles).
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes when run alone.
+"""
+import pytest
+import torch
+
+import oracle
+import shape_adaptive_tile_gb300 as sat
+import synth_inputs as si
+from tests import checks
+from tests.gpu_util import stream, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# dtype, M, N, K, family, alpha, beta
+CASES = [
+    ("bf16", 128, 8192, 8192, "dyadic", 1.5, 0.5),   # the dispatcher splits K: partial tiles in the scratch
+    ("tf32", 128, 8192, 8192, "normal", 1.0, 0.0),   # split K, beta 0 (C starts as NaN and is never read)
+    ("tf32", 300, 260, 200, "normal", 1.0, 0.0),     # no split: only the status word is scratch
+    ("fp16", 513, 264, 130, "dyadic", 1.0, 1.0),
+    ("bf16", 333, 517, 389, "uniform", 1.5, 0.5),    # misaligned row strides: plain-load producer
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    sat.build()
+    sat.lib()
+
+
+def _fresh_c(C0, M, N):
+    if C0 is None:
+        return torch.full((M, N), float("nan"), device="cuda")
+    return to_dev(C0)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}")
+def test_noalloc_matches_gemm_run_on_two_calls(case):
+    dtype, M, N, K, family, alpha, beta = case
+    A, B, C0 = si.problem(M, N, K, dtype, family, 21, "normal" if beta != 0 else None)
+    dA, dB = to_dev(A, dtype), to_dev(B, dtype)
+    ref = _fresh_c(C0, M, N)
+    with sat.Plan(M, N, K, dtype) as plan:
+        desc = plan.describe()
+        plan.run(dA, dB, ref, alpha, beta, stream())
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    ref_np = ref.cpu().numpy()
+    for call in range(2):
+        out = _fresh_c(C0, M, N)
+        rc = sat.gemm_run_noalloc(M, N, K, dtype, dA, dB, out, alpha, beta, stream())
+        assert rc == 0, sat.gemm_last_error()
+        torch.cuda.synchronize()
+        # Same kernel, same choice, fixed K order: the same bits as gemm_run.
+        checks.assert_bit_exact(out.cpu().numpy(), ref_np, f"gemm_run_noalloc call {call + 1} vs gemm_run [{desc}]")
+
+
+def test_noalloc_really_splits_k_for_the_skinny_case():
+    splits = int(sat.gemm_select_config(128, 8192, 8192, "bf16", torch.cuda.get_device_properties(0).multi_processor_count,
+                                        True).split(",")[4])
+    assert splits > 1
+
+
+def test_noalloc_rejects_a_problem_beyond_its_scratch():
+    # bf16 128 x 19456 x 8192 splits K 2 ways: 2 x 128 x 19456 floats = 19 MiB > 16 MiB.
+    M, N, K = 128, 19456, 8192
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    choice = sat.gemm_select_config(M, N, K, "bf16", sms, True).split(",")
+    if int(choice[4]) < 2:
+        pytest.skip(f"the dispatcher does not split this shape on {sms} SMs ({choice})")
+    x = torch.zeros(64, dtype=torch.bfloat16, device="cuda")   # never read: rejected before any launch
+    c = torch.zeros(64, device="cuda")
+    rc = sat.gemm_run_noalloc(M, N, K, "bf16", x, x, c, 1.0, 0.0, stream())
+    assert rc == -1
+    assert "scratch" in sat.gemm_last_error()
+    # and the entry point still works afterwards
+    A, B, _ = si.problem(64, 64, 64, "bf16", "dyadic", 3)
+    out = torch.empty(64, 64, device="cuda")
+    assert sat.gemm_run_noalloc(64, 64, 64, "bf16", to_dev(A, "bf16"), to_dev(B, "bf16"), out, 1.0, 0.0,
+                                stream()) == 0
+    torch.cuda.synchronize()
+    _, ref32 = oracle.gemm(A, B, None, 1.0, 0.0, "bf16")
+    checks.assert_bit_exact(out.cpu().numpy(), ref32, "after a rejected call")
+
+
+def test_noalloc_argument_errors():
+    x = torch.zeros(16, device="cuda")
+    assert sat.gemm_run_noalloc(-1, 4, 4, "tf32", x, x, x, 1.0, 0.0, stream()) == -1
+    assert sat.gemm_run_noalloc(4, 4, 4, "tf32", x, x, None, 1.0, 0.0, stream()) == -1
+    assert sat.gemm_run_noalloc(4, 4, 4, "tf32", x, x, x.data_ptr() + 2, 1.0, 0.0, stream()) == -3
+    assert sat.gemm_run_noalloc(0, 4, 4, "tf32", None, None, None, 1.0, 0.0, stream()) == 0
