@@ -76,8 +76,8 @@ struct Traits {
     // types the 128-byte swizzle with 32-byte atoms, the only MN-major
     // swizzle the tensor core takes for 32-bit operands. The plain-load
     // producer of tf32 instead stores B transposed, K-major like A.
-    static constexpr bool B_MN = !(kTF32 && PROD == kProdPlain);
-    static constexpr uint32_t B_LAYOUT = (kTF32 && B_MN) ? kLayoutSW128Atom32 : kLayoutSW128;
+    static constexpr bool B_MN = true;
+    static constexpr uint32_t B_LAYOUT = kTF32 ? kLayoutSW128Atom32 : kLayoutSW128;
     static constexpr uint32_t IDESC = idesc_f32acc(FMT, BM * CG, BN, B_MN);
     // MN-major: 128-byte column blocks are BK*128 bytes apart (leading byte
     // offset); K rows come in swizzle groups, 8 rows (1024 bytes) for the
@@ -298,8 +298,96 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 }
             }
         } else {
-            // Plain-load producer (1-SM): any row stride, 2- or 4-byte aligned.
-            using E = typename std::conditional<T::kTF32, uint32_t, uint16_t>::type;
+          if constexpr (T::kTF32) {
+            // Plain-load producer for 4-byte elements: asynchronous 4-byte
+            // copies straight into the swizzled stage layout (A K-major,
+            // B MN-major with 32-byte atoms: chunk c of row k at c ^ (k mod 4)),
+            // zero-filled outside the matrix. Each thread commits one copy
+            // group per fill and, STAGES - 1 fills later, waits for that
+            // group, makes it visible to the tensor core (proxy fence) and
+            // arrives on the fill's barrier.
+            const uint32_t* __restrict__ gA = static_cast<const uint32_t*>(args.A);
+            const uint32_t* __restrict__ gB = static_cast<const uint32_t*>(args.B);
+            constexpr int NP = T::NPW * 32;
+            static_assert(NP == 128 && T::BK == 32 && BN % NP == 0, "copy layout: 128 threads, 32-wide K");
+            constexpr int LAG = T::STAGES - 1;
+            constexpr int BCOLS = BN / NP;     // B columns per thread: n = p + 128 c
+            const int p = threadIdx.x;         // producer warps are warps 0..NPW-1
+            const int ak = p & 31;             // this thread's k within every A row
+            const int ar0 = p >> 5;            // its first A row; rows ar0 + 4 i
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int fills = 0, signalled = 0;
+            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+                const Unit w = unit_coord(t, args);
+                const int m0 = w.tm * T::BM;
+                const int n0 = w.tn * BN;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k0 = kb * T::BK;
+                    const uint32_t dA = sA + stage * T::A_BYTES;
+                    const uint32_t dB = sB + stage * T::B_BYTES;
+                    const int gk = k0 + ak;
+#pragma unroll 8
+                    for (int i = 0; i < T::BM / 4; ++i) {
+                        const int r = ar0 + 4 * i;
+                        const int gr = m0 + r;
+                        const bool v = gk < args.K && gr < args.M;
+                        const uint32_t* src = v ? gA + static_cast<int64_t>(gr) * args.K + gk : gA;
+                        cp_async_4(dA + static_cast<uint32_t>(r * 128 + ((((ak >> 2) ^ (r & 7)) << 4) | ((ak & 3) << 2))),
+                                   src, v ? 4u : 0u);
+                    }
+#pragma unroll
+                    for (int c = 0; c < BCOLS; ++c) {
+                        const int n = p + NP * c;
+                        const int gn = n0 + n;
+                        const int nn = n & 31;
+                        const uint32_t col = dB + static_cast<uint32_t>((n >> 5) * (T::BK * 128) + ((nn & 7) << 2));
+#pragma unroll 8
+                        for (int kr = 0; kr < T::BK; ++kr) {
+                            const int gk2 = k0 + kr;
+                            const bool v = gn < args.N && gk2 < args.K;
+                            const uint32_t* src = v ? gB + static_cast<int64_t>(gk2) * args.N + gn : gB;
+                            cp_async_4(col + static_cast<uint32_t>(kr * 128 + ((((nn >> 3) ^ (kr & 3)) << 5))), src,
+                                       v ? 4u : 0u);
+                        }
+                    }
+                    cp_async_commit();
+                    ++fills;
+                    if (fills - signalled > LAG) {
+                        cp_async_wait<LAG>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(full_bar(signalled % T::STAGES));
+                        ++signalled;
+                    }
+                    if (++stage == T::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy lands before the CTA moves on; signal the fills still open.
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            for (; signalled < fills; ++signalled)
+                mbar_arrive(full_bar(signalled % T::STAGES));
+            if (ok) {
+                for (int i = 0; i < T::STAGES; ++i) {
+                    if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer))
+                        break;
+                    if (++stage == T::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+          } else {
+            // Plain-load producer (1-SM, 2-byte elements): any row stride.
+            using E = uint16_t;
             const E* __restrict__ gA = static_cast<const E*>(args.A);
             const E* __restrict__ gB = static_cast<const E*>(args.B);
             constexpr int NP = T::NPW * 32;
@@ -359,10 +447,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         for (int i = 0; i < BATCH; ++i) {
                             const int idx = p + (i0 + i) * NP;
                             const int kr = idx / BN, n = idx - kr * BN;
-                            if constexpr (T::B_MN)
-                                *reinterpret_cast<E*>(dB + swz_mnmajor<T::ES, T::BK>(kr, n)) = v[i];
-                            else
-                                *reinterpret_cast<E*>(dB + swz_kmajor<T::ES>(n, kr)) = v[i];
+                            *reinterpret_cast<E*>(dB + swz_mnmajor<T::ES, T::BK>(kr, n)) = v[i];
                         }
                     }
                     fence_proxy_async_smem();
@@ -383,6 +468,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     }
                 }
             }
+          }
         }
     } else if (warp == T::MMA_WARP) {
         // ----------------------------------------------------------------- MMA
