@@ -553,13 +553,34 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         const float alpha = args.alpha, beta = args.beta;
         const int64_t ldc = args.N;
         constexpr int NCHUNK = BN / 32;
+        // C values (bulk-store path, beta != 0) of row (row0 + lane), columns
+        // gcol0 .. gcol0 + 31, as 8 aligned float4 loads; zero outside M x N.
+        auto load_c = [&](float (&cv)[32], int grow, int gcol0) {
+            const float4* src = reinterpret_cast<const float4*>(args.C + static_cast<int64_t>(grow) * ldc + gcol0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (grow < args.M && gcol0 + 4 * q < args.N)
+                    x = src[q];
+                cv[4 * q] = x.x;
+                cv[4 * q + 1] = x.y;
+                cv[4 * q + 2] = x.z;
+                cv[4 * q + 3] = x.w;
+            }
+        };
+        const bool prefetch_c = args.c_tma && beta != 0.0f;   // beta != 0 only unsplit
         for (int t = tile0; t < args.num_tiles; t += tile_step) {
-            if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
-                break;
-            tc_fence_after();
             const Unit w = unit_coord(t, args);
             const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
             const int n0 = w.tn * BN;
+            // Read the first chunk's C before waiting for the accumulator, so
+            // its latency overlaps the main loop; later chunks read theirs in turn.
+            float cv[32];
+            if (prefetch_c)
+                load_c(cv, row0 + lane, n0 + half * 32);
+            if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
+                break;
+            tc_fence_after();
             // Split s writes its slice of the output: rows s * out_rows + row.
             const int yoff = w.s * args.out_rows;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
@@ -588,21 +609,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     // group of 8 lanes covers all 32 banks) and let one lane
                     // hand the chunk to the TMA engine, which clips it to M x N.
                     const int grow = row0 + lane;
-                    float cv[32];
-                    if (beta != 0.0f) {
-                        const float4* src = reinterpret_cast<const float4*>(
-                            args.C + static_cast<int64_t>(grow) * ldc + gcol0);  // beta != 0 only unsplit
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (grow < args.M && gcol0 + 4 * q < args.N)
-                                x = src[q];
-                            cv[4 * q] = x.x;
-                            cv[4 * q + 1] = x.y;
-                            cv[4 * q + 2] = x.z;
-                            cv[4 * q + 3] = x.w;
-                        }
-                    }
+                    if (prefetch_c && c != half)
+                        load_c(cv, grow, gcol0);
                     if (lane == 0)
                         bulk_wait_read<0>();  // the previous store has finished reading the buffer
                     __syncwarp();

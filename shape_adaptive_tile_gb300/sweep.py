@@ -47,16 +47,16 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152):
     return out
 
 
-def time_config(sat, torch, M, N, K, dtype, config, dA, dB, dC, flush, runs, warmup):
+def time_config(sat, torch, M, N, K, dtype, config, dA, dB, dC, flush, runs, warmup, alpha=1.0, beta=0.0):
     stream = torch.cuda.current_stream()
     with sat.Plan(M, N, K, dtype, config) as plan:
         for _ in range(warmup):
-            plan.run(dA, dB, dC, 1.0, 0.0, stream.cuda_stream)
+            plan.run(dA, dB, dC, alpha, beta, stream.cuda_stream)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
         for e0, e1 in ev:
             flush.zero_()
             e0.record(stream)
-            plan.run(dA, dB, dC, 1.0, 0.0, stream.cuda_stream)
+            plan.run(dA, dB, dC, alpha, beta, stream.cuda_stream)
             e1.record(stream)
         torch.cuda.synchronize()
         sat.check(plan.status())
@@ -64,23 +64,25 @@ def time_config(sat, torch, M, N, K, dtype, config, dA, dB, dC, flush, runs, war
         return {"config": config, "plan": plan.describe(), "median_ms": statistics.median(t), "min_ms": t[0]}
 
 
-def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None):
+def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None, alpha=1.0, beta=0.0):
     es = 4 if dtype == "tf32" else 2
     tma_ok = (K * es) % 16 == 0 and (N * es) % 16 == 0
     rng = np.random.default_rng(0)
     tdt = {"tf32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
     dA = torch.from_numpy(rng.integers(-4, 5, (M, K)).astype(np.float32)).to("cuda", tdt)
     dB = torch.from_numpy(rng.integers(-4, 5, (K, N)).astype(np.float32)).to("cuda", tdt)
-    dC = torch.empty(M, N, device="cuda")
+    # C starts finite; with beta != 0 it is read (and C = alpha*A*B + beta*C stays bounded).
+    dC = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to("cuda")
     flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
     res = []
     for cfg in configs or candidates(M, N, K, dtype, tma_ok):
-        r = time_config(sat, torch, M, N, K, dtype, cfg, dA, dB, dC, flush, runs, warmup)
+        r = time_config(sat, torch, M, N, K, dtype, cfg, dA, dB, dC, flush, runs, warmup, alpha, beta)
         r["tflops"] = 2.0 * M * N * K / (r["median_ms"] * 1e-3) / 1e12
         res.append(r)
     with sat.Plan(M, N, K, dtype) as p:
         chosen = p.describe()
-    return {"dtype": dtype, "M": M, "N": N, "K": K, "results": res, "dispatcher": chosen}
+    return {"dtype": dtype, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta, "results": res,
+            "dispatcher": chosen}
 
 
 def write_table(entries, path=TABLE):
@@ -102,7 +104,8 @@ def write_table(entries, path=TABLE):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", required=True)
-    ap.add_argument("--shapes", nargs="*", help="dtype:MxNxK (default: every benchmark workload)")
+    ap.add_argument("--shapes", nargs="*",
+                    help="dtype:MxNxK[:beta] (default: every benchmark workload, with its own alpha and beta)")
     ap.add_argument("--configs", nargs="*", help="restrict to these configurations")
     ap.add_argument("--runs", type=int, default=30)
     ap.add_argument("--table", action="store_true", help="also write csrc/sweep_table.inc")
@@ -116,15 +119,16 @@ def main(argv=None):
     if args.shapes:
         shapes = []
         for s in args.shapes:
-            dt, dims = s.split(":")
-            shapes.append((dt, tuple(int(x) for x in dims.split("x"))))
+            parts = s.split(":")
+            beta = float(parts[2]) if len(parts) > 2 else 0.0
+            shapes.append((parts[0], tuple(int(x) for x in parts[1].split("x")), 1.0 if beta == 0 else 1.5, beta))
     else:
-        shapes = sorted({(w[1], w[2]) for w in si.WORKLOADS})
+        shapes = sorted({(w[1], w[2], w[4], w[5]) for w in si.WORKLOADS})
     entries = []
-    for dt, (M, N, K) in shapes:
-        e = sweep_shape(sat, torch, M, N, K, dt, args.runs, configs=args.configs)
+    for dt, (M, N, K), alpha, beta in shapes:
+        e = sweep_shape(sat, torch, M, N, K, dt, args.runs, configs=args.configs, alpha=alpha, beta=beta)
         best = min(e["results"], key=lambda r: r["median_ms"])
-        print(f"{dt} {M}x{N}x{K}: best {best['config']} {best['tflops']:.1f} TFLOP/s; "
+        print(f"{dt} {M}x{N}x{K} beta {beta:g}: best {best['config']} {best['tflops']:.1f} TFLOP/s; "
               f"dispatcher [{e['dispatcher']}]", flush=True)
         for r in sorted(e["results"], key=lambda r: r["median_ms"])[:5]:
             print(f"    {r['config']:>12} {r['median_ms'] * 1e3:9.1f} us {r['tflops']:8.1f} TFLOP/s", flush=True)
