@@ -24,8 +24,8 @@ pytestmark = pytest.mark.gpu
 
 # dtype, M, N, K, family, alpha, beta
 CASES = [
-    ("bf16", 128, 8192, 8192, "dyadic", 1.5, 0.5),   # the dispatcher splits K: partial tiles in the scratch
-    ("tf32", 128, 8192, 8192, "normal", 1.0, 0.0),   # split K, beta 0 (C starts as NaN and is never read)
+    ("bf16", 256, 4096, 8192, "dyadic", 1.5, 0.5),   # CTA pairs, K split 2 ways: partial tiles in the scratch
+    ("tf32", 128, 2048, 16384, "normal", 1.0, 0.0),  # K split 4 ways, beta 0 (C starts as NaN, never read)
     ("tf32", 300, 260, 200, "normal", 1.0, 0.0),     # no split: only the status word is scratch
     ("fp16", 513, 264, 130, "dyadic", 1.0, 1.0),
     ("bf16", 333, 517, 389, "uniform", 1.5, 0.5),    # misaligned row strides: plain-load producer
@@ -67,19 +67,27 @@ def test_noalloc_matches_gemm_run_on_two_calls(case):
         checks.assert_bit_exact(out.cpu().numpy(), ref_np, f"gemm_run_noalloc call {call + 1} vs gemm_run [{desc}]")
 
 
-def test_noalloc_really_splits_k_for_the_skinny_case():
-    splits = int(sat.gemm_select_config(128, 8192, 8192, "bf16", torch.cuda.get_device_properties(0).multi_processor_count,
-                                        True).split(",")[4])
-    assert splits > 1
-
-
-def test_noalloc_rejects_a_problem_beyond_its_scratch():
-    # bf16 128 x 19456 x 8192 splits K 2 ways: 2 x 128 x 19456 floats = 19 MiB > 16 MiB.
-    M, N, K = 128, 19456, 8192
+def _split_workspace_bytes(M, N, K, dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    choice = sat.gemm_select_config(M, N, K, "bf16", sms, True).split(",")
-    if int(choice[4]) < 2:
-        pytest.skip(f"the dispatcher does not split this shape on {sms} SMs ({choice})")
+    bn, cg, _, _, splits, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
+    rows = 128 * int(cg)
+    return int(splits), int(splits) * (-(-M // rows) * rows) * N * 4
+
+
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 256, 4096, 8192), ("tf32", 128, 2048, 16384)])
+def test_noalloc_cases_really_split_k_within_the_scratch(dtype, M, N, K):
+    splits, ws = _split_workspace_bytes(M, N, K, dtype)
+    assert splits > 1 and ws <= (16 << 20) - 256
+
+
+# bf16 128 x 19456 x 8192 splits K 2 ways (19 MiB of partial tiles); the
+# benchmark's bf16 128 x 8192 x 8192 splits 4 ways (16 MiB): both exceed the
+# 16 MiB - 256 bytes of workspace.
+@pytest.mark.parametrize("M,N,K", [(128, 19456, 8192), (128, 8192, 8192)])
+def test_noalloc_rejects_a_problem_beyond_its_scratch(M, N, K):
+    splits, ws = _split_workspace_bytes(M, N, K, "bf16")
+    if splits < 2 or ws <= (16 << 20) - 256:
+        pytest.skip(f"the dispatcher does not need more scratch than the array holds here ({splits}, {ws})")
     x = torch.zeros(64, dtype=torch.bfloat16, device="cuda")   # never read: rejected before any launch
     c = torch.zeros(64, device="cuda")
     rc = sat.gemm_run_noalloc(M, N, K, "bf16", x, x, c, 1.0, 0.0, stream())
