@@ -195,6 +195,25 @@ def run_reference(args, w, rank, world):
 
 
 # ----------------------------------------------------------------- our arm
+def job_time_ms(local_ms, world, torch, device=None):
+    """Whole-job time of the timed steps: the slowest rank's (max over ranks).
+
+    Every rank runs its own replica of the GEMM (the path has no exchange
+    step), so the job finishes when the slowest rank does."""
+    if world <= 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_step, steps, job_ms, world):
+    """Whole-job TFLOP/s: the work of all ranks over the job time, and the
+    per-step time."""
+    ms = job_ms / steps
+    return world * flops_per_step / (ms * 1e-3) / 1e12, ms
+
+
 def traffic_for(desc):
     """DRAM bytes per launch recorded from an ncu capture of this exact
     kernel source, or None (no capture, or the source changed since)."""
@@ -262,11 +281,7 @@ def bench_one(args, w, rank, world, torch, sat, quiet=False):
         time.sleep(0.2)
         clocks.stop()
     times = [e0.elapsed_time(e1) for e0, e1 in ev]
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_time_ms(sum(times), world, torch, dev)
     sat.check(plan.status())
     res = {"plan": desc, "flops": flops, "times_ms": times, "total_ms": total_ms, "launches": launches,
            "clocks": clocks.summary() if clocks else None, "dtype": dt, "M": M, "N": N, "K": K,
@@ -361,8 +376,7 @@ def main():
 
     r = bench_one(args, w, rank, world, torch, sat)
     pk, pk_src = peaks()
-    ms = r["total_ms"] / args.steps
-    value = world * r["flops"] / (ms * 1e-3) / 1e12
+    value, ms = job_value(r["flops"], args.steps, r["total_ms"], world)
     peak = tensor_peak(r["dtype"], pk)
     achieved = r["flops"] / (ms * 1e-3) / 1e12
     line = {

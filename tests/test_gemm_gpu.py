@@ -55,6 +55,20 @@ def test_config_normal_rel_rms(dtype, config):
     checks.assert_rel_rms(got, ref64, si.REL_RMS_BOUND[dtype], f"{dtype} [{desc}]")
 
 
+# Extreme aspect ratios through the dispatcher's own choice: a K loop of 2048+
+# k-blocks, tall and wide outputs with ragged tails, single rows and columns
+# (N = 1 rules out TMA for B). Dyadic inputs keep every sum exact in fp32
+# (|sum| <= 16 K < 2^24), so the comparison is bit for bit.
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 128, 128, 131072), ("tf32", 65537, 64, 96),
+                                         ("fp16", 64, 65600, 40), ("tf32", 1, 4096, 4096),
+                                         ("bf16", 4096, 1, 64), ("tf32", 3, 5, 70000)])
+def test_extreme_aspect_ratios_dyadic_exact(dtype, M, N, K):
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 31, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5)
+    checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_beta_zero_ignores_nan_c(dtype):
     M, N, K = 200, 300, 100
