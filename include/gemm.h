@@ -67,8 +67,9 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
  * `config` = "bn,cg,raster,group[,splits]" (bn in {64,128,256}; cg 1 or 2,
  * where 2 needs bn >= 128; raster 0 = groups along M, 1 = along N;
  * group >= 1; splits 1..16 K splits, default 1), optionally followed by
- * ",plain" to force the plain-load producer. NULL or "" means the dispatcher
- * decides. For sweeps and tests; every configuration computes the same GEMM
+ * ",cload" (with beta != 0 the epilogue loads C itself instead of the
+ * producer fetching it through the operand ring) and ",plain" (force the
+ * plain-load producer). NULL or "" means the dispatcher decides. For sweeps and tests; every configuration computes the same GEMM
  * (with splits > 1 the K sum is split into fixed slices whose partial tiles
  * are added in fixed order, so the bits can differ from splits = 1 but are
  * identical from run to run).
@@ -177,9 +178,12 @@ int gemm_selftest_bounded_wait(uint64_t timeout_ns);
  * Host-only view of the dispatcher (no device is touched): the choice that
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
- * strides are multiples of 16 bytes). Writes "bn,cg,raster,group,splits,source"
- * (source: rule or table) into `out` (NUL-terminated, at most `out_len`
- * bytes). Returns 0, or GEMM_ERR_ARG on bad arguments.
+ * strides are multiples of 16 bytes). Writes
+ * "bn,cg,raster,group,splits,cload,source" (cload: 1 if, with beta != 0, the
+ * epilogue loads C itself, 0 if the producer fetches it through the operand
+ * ring where the kernel allows; source: rule or table) into `out`
+ * (NUL-terminated, at most `out_len` bytes). Returns 0, or GEMM_ERR_ARG on
+ * bad arguments.
  */
 int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int sm_count, int tma_ok, char* out,
                        int out_len);

@@ -96,6 +96,7 @@ struct gemm_plan {
     int sm_count = 0;
     sat::Choice choice{};
     bool force_plain = false;
+    bool c_ring = false;  // beta != 0: the producer fetches C through the operand ring
     const sat::KernelEntry* tma = nullptr;    // null when the strides rule out TMA
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
     int grid_tma = 0, grid_plain = 0;
@@ -182,16 +183,26 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     if (config && config[0]) {
         char head[64];
         std::snprintf(head, sizeof head, "%s", config);
+        // Optional tags after the numbers, in this order: ",cload" (the
+        // epilogue loads C itself), ",plain" (plain-load producer).
         char* plain_tag = std::strstr(head, ",plain");
         if (plain_tag) {
             *plain_tag = '\0';
             p->force_plain = true;
         }
+        char* cload_tag = std::strstr(head, ",cload");
+        bool cload = false;
+        if (cload_tag) {
+            *cload_tag = '\0';
+            cload = true;
+        }
         if (!sat::parse_choice(head, &p->choice)) {
-            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (want \"bn,cg,raster,group[,plain]\")", config);
+            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (want \"bn,cg,raster,group[,splits][,cload][,plain]\")",
+                 config);
             delete p;
             return nullptr;
         }
+        p->choice.cload = cload ? 1 : 0;
         source = "forced";
     } else {
         p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
@@ -263,10 +274,11 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
     const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
-    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s",
+    p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1;
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
                   p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
-                  source);
+                  source, p->c_ring ? " cring" : "");
     return p;
 }
 
@@ -363,6 +375,7 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
     const bool c_tma = split ? p->ws_tma : (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
+    a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
     CUtensorMap tmA{}, tmB{}, tmC{};
     if (split && c_tma) {
         tmC = p->tmW;
@@ -491,8 +504,8 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
         return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
     const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
-    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
-                  c.splits > 1 ? c.splits : 1, c.source == 1 ? "table" : "rule");
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.splits > 1 ? c.splits : 1, c.cload, c.source == 1 ? "table" : "rule");
     return GEMM_OK;
 }
 

@@ -110,6 +110,11 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     best.group = best.cg == 2 ? 4 : 8;
     best.source = 0;
     best.splits = 1;
+    // beta != 0: fetching C through the operand ring pays when C is a large
+    // share of a tile's traffic (short K); with a long K loop the epilogue's
+    // own C loads hide behind the next tile's main loop, and the ring stages
+    // that C would hold are worth more to the operands.
+    best.cload = cdiv(K, dt == 0 ? 32 : 64) > 32 ? 1 : 0;
     // Split K when the chosen tiles would leave most SMs idle and K is long:
     // each split needs at least 16 k-blocks, and the fixed-order reduction
     // (S + 2 floats of traffic per output) plus its launch must pay off.

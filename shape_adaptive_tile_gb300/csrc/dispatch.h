@@ -12,13 +12,15 @@ struct Choice {
     int group;    // raster group size in tiles
     int source;   // 0: analytic rule, 1: committed sweep table, 2: forced
     int splits;   // K splits (fixed-order reduction through a workspace); 0 or 1: none
+    int cload;    // beta != 0: 1 = the epilogue loads C itself, 0 = the producer fetches it through the ring
 };
 
 // Picks tile and schedule. `tma_ok` says whether the TMA load path can be
 // used (16-byte-multiple row strides); when false only 1-SM tiles exist.
 Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool tma_ok);
 
-// Override for sweeps and tests: "bn,cg,raster,group[,splits]" (e.g. "256,2,0,8").
+// Override for sweeps and tests: "bn,cg,raster,group[,splits]" (e.g. "256,2,0,8");
+// tags such as ",cload" are stripped by the caller first.
 // Returns false if `spec` is malformed.
 bool parse_choice(const char* spec, Choice* out);
 

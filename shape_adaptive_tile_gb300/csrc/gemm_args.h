@@ -29,6 +29,7 @@ struct GemmArgs {
     int group;                 // rasterisation group size (>= 1)
     int raster;                // 0: groups along M, 1: groups along N
     int c_tma;                 // 1: C is written (and read) through the TMA store path
+    int c_ring;                // 1: the producer also fetches each tile's C (beta != 0) through the ring
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;
 };

@@ -60,7 +60,7 @@ struct Traits {
     static constexpr int EPI_WARPS = PROD == kProdTMA ? 8 : 4;   // plain-load CTAs keep 9 warps
     static constexpr int EPI_WARP_BYTES = 4096;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -69,6 +69,14 @@ struct Traits {
     static constexpr int EPI_WARP0 = NPW + 1;
     static constexpr int THREADS = (NPW + 1 + EPI_WARPS) * 32;
     static constexpr int ACC_COLS = BN;             // fp32 accumulator: one column per element
+    // beta != 0: the producer can fetch each tile's C (this CTA's BM x BN
+    // fp32 block, as 32 x 32 chunks of 4 KB in the 128-byte swizzle) through
+    // the operand ring, right after the tile's k-blocks: CPS chunks per
+    // stage, NCS stages per tile, at least two stages left for k-blocks.
+    static constexpr int C_CHUNKS = (BM / 32) * (BN / 32);
+    static constexpr int CPS = STAGE_BYTES / 4096;
+    static constexpr int NCS = (C_CHUNKS + CPS - 1) / CPS;
+    static constexpr bool C_RING_OK = PROD == kProdTMA && NCS + 2 <= STAGES;
     static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     static constexpr uint32_t FMT = DT == kDtTF32 ? kFmtTF32 : DT == kDtBF16 ? kFmtBF16 : kFmtF16;
     // B in shared memory. TMA copies B as it lies in memory (N contiguous,
@@ -184,6 +192,18 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     const uint32_t tmem_ready_bar = bars + 8u * (2 * T::STAGES + 5);   // pair: the peer's TMEM is allocated
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbars + 8 * (2 * T::STAGES + 6));
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbars + 8 * (2 * T::STAGES + 6) + 4);
+    // C through the ring: per stage, a barrier for its C fill and a count of
+    // the epilogue warps that have read their chunk of it.
+    auto cfull_bar = [&](int s) { return bars + 8u * (2 * T::STAGES + 7 + s); };
+    int* const c_readers = reinterpret_cast<int*>(gbars + 8 * (3 * T::STAGES + 7));
+    static_assert(8 * (3 * T::STAGES + 7) + 4 * T::STAGES <= T::BAR_BYTES, "barrier area");
+    // Shared address of 4 KB slot j of ring stage s (its A part, then its B part).
+    auto ring_slot = [&](int s, int j) -> uint32_t {
+        constexpr int AS = T::A_BYTES / 4096;
+        return j < AS ? sA + static_cast<uint32_t>(s * T::A_BYTES + j * 4096)
+                      : sB + static_cast<uint32_t>(s * T::B_BYTES + (j - AS) * 4096);
+    };
+    const bool c_ring = T::C_RING_OK && args.c_ring != 0 && args.c_tma != 0 && args.splits == 1 && args.beta != 0.0f;
 
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
@@ -196,6 +216,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), T::EPI_WARPS * CG);
+        }
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(cfull_bar(s), 1);
+            c_readers[s] = 0;
         }
         mbar_init(drain_bar, 1);
         mbar_init(tmem_ready_bar, 1);
@@ -281,6 +305,31 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         if (++stage == T::STAGES) {
                             stage = 0;
                             phase ^= 1u;
+                        }
+                    }
+                    // Then this CTA's rows of the tile's C, column chunk by
+                    // column chunk (the order the epilogue reads them in),
+                    // each stage completing on this CTA's own cfull barrier.
+                    if (ok && c_ring) {
+                        const int crow = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
+                        const int ccol = w.tn * BN;
+                        for (int cs = 0; cs < T::NCS; ++cs) {
+                            if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
+                                ok = false;
+                                break;
+                            }
+                            const int first = cs * T::CPS;
+                            const int n = min(T::CPS, T::C_CHUNKS - first);
+                            mbar_arrive_expect_tx(cfull_bar(stage), static_cast<uint32_t>(n) * 4096u);
+                            for (int j = 0; j < n; ++j) {
+                                const int id = first + j;
+                                const int cc = id / (T::BM / 32), rb = id - cc * (T::BM / 32);
+                                tma_load_2d(ring_slot(stage, j), &tmC, cfull_bar(stage), ccol + cc * 32, crow + rb * 32);
+                            }
+                            if (++stage == T::STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                 }
@@ -474,7 +523,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         // ----------------------------------------------------------------- MMA
         if (leader && lane == 0) {
             int stage = 0;
-            uint32_t phase = 0;
+            uint32_t fpar = 0;  // per stage: parity of its next k-block fill (C fills skip the full barrier)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued = false;
@@ -489,10 +538,11 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
                 const Unit w = unit_coord(t, args);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bar<false>(full_bar(stage), phase, wc, kErrTimeoutMma)) {
+                    if (!wait_bar<false>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma)) {
                         ok = false;
                         break;
                     }
+                    fpar ^= 1u << stage;
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * T::A_BYTES;
                     const uint32_t b0 = sB + stage * T::B_BYTES;
@@ -507,10 +557,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         mma_commit(empty_bar(stage));
                     else
                         mma_commit_pair(empty_bar(stage), 0x3);
-                    if (++stage == T::STAGES) {
+                    if (++stage == T::STAGES)
                         stage = 0;
-                        phase ^= 1u;
-                    }
                 }
                 if (!ok)
                     break;
@@ -518,6 +566,11 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     mma_commit(tfull_bar(acc));
                 else
                     mma_commit_pair(tfull_bar(acc), 0x3);
+                if (c_ring) {  // the tile's C stages go to the epilogue
+                    stage += T::NCS;
+                    if (stage >= T::STAGES)
+                        stage -= T::STAGES;
+                }
                 acc ^= 1;
                 if (acc == 0)
                     acc_phase ^= 1u;
@@ -568,97 +621,162 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 cv[4 * q + 3] = x.w;
             }
         };
-        const bool prefetch_c = args.c_tma && beta != 0.0f;   // beta != 0 only unsplit
-        for (int t = tile0; t < args.num_tiles; t += tile_step) {
-            const Unit w = unit_coord(t, args);
-            const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
-            const int n0 = w.tn * BN;
-            // Read the first chunk's C before waiting for the accumulator, so
-            // its latency overlaps the main loop; later chunks read theirs in turn.
-            float cv[32];
-            if (prefetch_c)
-                load_c(cv, row0 + lane, n0 + half * 32);
-            if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
-                break;
-            tc_fence_after();
-            // Split s writes its slice of the output: rows s * out_rows + row.
-            const int yoff = w.s * args.out_rows;
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
-                                   static_cast<uint32_t>(acc * T::ACC_COLS);
+        // The tile loop, compiled twice: with C through the ring, and with C
+        // loaded by the epilogue (or not read), so that each copy keeps only
+        // the registers its own path needs.
+        auto tile_loop = [&](auto ring_tag) {
+            constexpr bool RING = decltype(ring_tag)::value;
+            const bool prefetch_c = !RING && args.c_tma && beta != 0.0f;   // beta != 0 only unsplit
+            // C through the ring: where the next unit's stages start, and per
+            // stage the parity of its next C fill.
+            int rpos = 0;
+            uint32_t cpar = 0;
+            bool ok = true;
+            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+                const Unit w = unit_coord(t, args);
+                const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
+                const int n0 = w.tn * BN;
+                int cst = 0;  // ring stage holding this tile's first C chunks
+                if constexpr (RING) {
+                    cst = (rpos + (w.kb1 - w.kb0)) % T::STAGES;
+                    rpos = (cst + T::NCS) % T::STAGES;
+                }
+                // Read the first chunk's C before waiting for the accumulator, so
+                // its latency overlaps the main loop; later chunks read theirs in turn.
+                float cv[32];
+                if constexpr (!RING) {
+                    if (prefetch_c)
+                        load_c(cv, row0 + lane, n0 + half * 32);
+                }
+                if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
+                    break;
+                tc_fence_after();
+                // Split s writes its slice of the output: rows s * out_rows + row.
+                const int yoff = w.s * args.out_rows;
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
+                                       static_cast<uint32_t>(acc * T::ACC_COLS);
 #pragma unroll 1
-            for (int c = half; c < NCHUNK; c += CSTEP) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, r);
-                tmem_wait_ld();
-                if (c + CSTEP >= NCHUNK) {
-                    // This warp's TMEM reads of the accumulator are done: hand it back.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 1)
-                            mbar_arrive(tempty0 + 8u * acc);
-                        else
-                            mbar_arrive_cluster(tempty0 + 8u * acc);
-                    }
-                }
-                const int gcol0 = n0 + c * 32;
-                if (args.c_tma) {
-                    // Bulk-store path: this thread owns row (row0 + lane) of the
-                    // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
-                    // (16-byte piece q of row l at position q ^ (l & 7): each
-                    // group of 8 lanes covers all 32 banks) and let one lane
-                    // hand the chunk to the TMA engine, which clips it to M x N.
-                    const int grow = row0 + lane;
-                    if (prefetch_c && c != half)
-                        load_c(cv, grow, gcol0);
-                    if (lane == 0)
-                        bulk_wait_read<0>();  // the previous store has finished reading the buffer
-                    __syncwarp();
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            v[e] = alpha * __uint_as_float(r[4 * q + e]);
-                            if (beta != 0.0f)
-                                v[e] = fmaf(beta, cv[4 * q + e], v[e]);
+                for (int c = half; c < NCHUNK; c += CSTEP) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, r);
+                    tmem_wait_ld();
+                    if (c + CSTEP >= NCHUNK) {
+                        // This warp's TMEM reads of the accumulator are done: hand it back.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (CG == 1)
+                                mbar_arrive(tempty0 + 8u * acc);
+                            else
+                                mbar_arrive_cluster(tempty0 + 8u * acc);
                         }
-                        st_shared_v4(sb + static_cast<uint32_t>(lane * 128 + ((q ^ (lane & 7)) << 4)), v[0], v[1],
-                                     v[2], v[3]);
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && row0 < args.M && gcol0 < args.N) {
-                        tma_store_2d(&tmC, sb, gcol0, yoff + row0);
-                        bulk_commit();
-                    }
-                    continue;
-                }
-                // Row-store fallback: transpose through the XOR-swizzled
-                // buffer (element (row l, column j) at l*32 + (j ^ l): conflict
-                // free both ways), then each row is written by the warp as 32
-                // consecutive floats, masked to M x N.
+                    const int gcol0 = n0 + c * 32;
+                    if (args.c_tma) {
+                        // Bulk-store path: this thread owns row (row0 + lane) of the
+                        // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
+                        // (16-byte piece q of row l at position q ^ (l & 7): each
+                        // group of 8 lanes covers all 32 banks) and let one lane
+                        // hand the chunk to the TMA engine, which clips it to M x N.
+                        const int grow = row0 + lane;
+                        // C through the ring: chunk (column chunk c, row block sub)
+                        // of the tile's C, in the same swizzle, in slot csrc of
+                        // stage cst_c once its fill has landed.
+                        int cs = 0, cst_c = 0;
+                        uint32_t csrc = 0;
+                        if constexpr (RING) {
+                            const int id = c * (T::BM / 32) + sub;
+                            cs = id / T::CPS;
+                            cst_c = cst + cs < T::STAGES ? cst + cs : cst + cs - T::STAGES;
+                            if (!wait_bar<false>(cfull_bar(cst_c), (cpar >> cst_c) & 1u, wc, kErrTimeoutEpilogue)) {
+                                ok = false;
+                                break;
+                            }
+                            csrc = ring_slot(cst_c, id - cs * T::CPS) + static_cast<uint32_t>(lane * 128);
+                        } else if (prefetch_c && c != half) {
+                            load_c(cv, grow, gcol0);
+                        }
+                        if (lane == 0)
+                            bulk_wait_read<0>();  // the previous store has finished reading the buffer
+                        __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    buf[lane * 32 + (j ^ lane)] = __uint_as_float(r[j]);
-                __syncwarp();
-                const int col = gcol0 + lane;
-                if (col < args.N) {
-                    float* cp = args.C + (static_cast<int64_t>(yoff) + row0) * ldc + col;
-                    const int rows = min(32, args.M - row0);
-#pragma unroll 4
-                    for (int i = 0; i < rows; ++i) {
-                        float v = alpha * buf[i * 32 + (lane ^ i)];
-                        if (beta != 0.0f)
-                            v = fmaf(beta, cp[i * ldc], v);
-                        cp[i * ldc] = v;
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t piece = static_cast<uint32_t>((q ^ (lane & 7)) << 4);
+                            float v[4], cq[4];
+                            if constexpr (RING) {
+                                ld_shared_v4(csrc + piece, cq[0], cq[1], cq[2], cq[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    cq[e] = cv[4 * q + e];
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                v[e] = alpha * __uint_as_float(r[4 * q + e]);
+                                if (beta != 0.0f)
+                                    v[e] = fmaf(beta, cq[e], v[e]);
+                            }
+                            st_shared_v4(sb + static_cast<uint32_t>(lane * 128) + piece, v[0], v[1], v[2], v[3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (row0 < args.M && gcol0 < args.N) {
+                                tma_store_2d(&tmC, sb, gcol0, yoff + row0);
+                                bulk_commit();
+                            }
+                            // This warp has read its chunk of the C stage; the
+                            // stage's last reader hands it back to the producer.
+                            if constexpr (RING) {
+                                const int readers = min(T::CPS, T::C_CHUNKS - cs * T::CPS);
+                                __threadfence_block();
+                                if (atomicAdd(&c_readers[cst_c], 1) == readers - 1) {
+                                    atomicSub(&c_readers[cst_c], readers);
+                                    __threadfence_block();
+                                    mbar_arrive(empty_bar(cst_c));
+                                }
+                            }
+                        }
+                        continue;
                     }
+                    // Row-store fallback: transpose through the XOR-swizzled
+                    // buffer (element (row l, column j) at l*32 + (j ^ l): conflict
+                    // free both ways), then each row is written by the warp as 32
+                    // consecutive floats, masked to M x N.
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        buf[lane * 32 + (j ^ lane)] = __uint_as_float(r[j]);
+                    __syncwarp();
+                    const int col = gcol0 + lane;
+                    if (col < args.N) {
+                        float* cp = args.C + (static_cast<int64_t>(yoff) + row0) * ldc + col;
+                        const int rows = min(32, args.M - row0);
+#pragma unroll 4
+                        for (int i = 0; i < rows; ++i) {
+                            float v = alpha * buf[i * 32 + (lane ^ i)];
+                            if (beta != 0.0f)
+                                v = fmaf(beta, cp[i * ldc], v);
+                            cp[i * ldc] = v;
+                        }
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
+                if constexpr (RING) {
+                    for (int cs = 0; cs < T::NCS; ++cs)
+                        cpar ^= 1u << (cst + cs < T::STAGES ? cst + cs : cst + cs - T::STAGES);
+                }
+                acc ^= 1;
+                if (acc == 0)
+                    acc_phase ^= 1u;
             }
-            acc ^= 1;
-            if (acc == 0)
-                acc_phase ^= 1u;
+        };
+        if constexpr (T::C_RING_OK) {
+            if (c_ring)
+                tile_loop(std::true_type{});
+            else
+                tile_loop(std::false_type{});
+        } else {
+            tile_loop(std::false_type{});
         }
         if (args.c_tma && lane == 0)
             bulk_wait<0>();  // every bulk store of this warp has completed

@@ -79,6 +79,7 @@ constexpr KernelEntry make_entry()
                        T::BK,
                        T::B_LAYOUT == kLayoutSW128Atom32 ? static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)
                                                          : static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B),
+                       T::C_RING_OK ? 1 : 0,
                        &prepare_variant<DT, BN, CG, PROD>, &max_clusters_variant<DT, BN, CG, PROD>,
                        &launch_variant<DT, BN, CG, PROD>};
 }

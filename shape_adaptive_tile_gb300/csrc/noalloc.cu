@@ -238,6 +238,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
                          CU_TENSOR_MAP_SWIZZLE_128B))
         return fail(GEMM_ERR_LAUNCH, "encoding the output tensor map");
     a.c_tma = c_tma ? 1 : 0;
+    a.c_ring = !c.cload && use_tma && k->c_ring && c_tma && splits == 1 && beta != 0.0f ? 1 : 0;
     if (use_tma) {
         if (!encode(&tmA, tdt, es, A, K, M, static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tmB, tdt, es, B, N, K, static_cast<uint32_t>(128 / es), static_cast<uint32_t>(k->bk),

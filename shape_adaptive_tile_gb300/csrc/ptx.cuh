@@ -234,6 +234,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
                  : "memory");
 }
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float& a, float& b, float& c, float& d)
+{
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr) : "memory");
+}
+
 // ---- tcgen05: tensor memory --------------------------------------------------
 
 template <int CG>

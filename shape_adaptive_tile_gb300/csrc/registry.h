@@ -19,6 +19,7 @@ struct KernelEntry {
     int smem;      // dynamic shared memory bytes
     int bk;        // K per stage
     int b_swizzle; // CUtensorMapSwizzle of B's tensor map
+    int c_ring;    // 1: with beta != 0 the producer can fetch C through the operand ring
     cudaError_t (*prepare)();  // sets the kernel's dynamic shared-memory limit
     int (*max_clusters)();     // co-resident CTA pairs on this device (cg == 2), 0 if unknown
     cudaError_t (*launch)(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,

@@ -20,6 +20,7 @@ import argparse
 import itertools
 import json
 import os
+import re
 import statistics
 import sys
 
@@ -30,7 +31,7 @@ TABLE = os.path.join(HERE, "csrc", "sweep_table.inc")
 DT_CODE = {"tf32": 0, "bf16": 1, "fp16": 2}
 
 
-def candidates(M, N, K, dtype, tma_ok, sm_count=152):
+def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
     out = []
     kb = -(-K // (32 if dtype == "tf32" else 64))
     for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
@@ -38,6 +39,11 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152):
             continue
         for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
             out.append(f"{bn},{cg},{raster},{group}")
+            # beta != 0: also with the epilogue loading C itself instead of
+            # the producer fetching it through the ring (the 1-SM 256-wide
+            # tile has no ring stages to spare, so it always loads C itself)
+            if beta != 0.0 and tma_ok and (bn, cg) != (256, 1):
+                out.append(f"{bn},{cg},{raster},{group},cload")
         # K splits only where the tiles alone leave at least half the SMs idle
         ctas = -(-M // (128 * cg)) * -(-N // bn) * cg
         for s in (2, 4, 8):
@@ -75,7 +81,7 @@ def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None, alp
     dC = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to("cuda")
     flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
     res = []
-    for cfg in configs or candidates(M, N, K, dtype, tma_ok):
+    for cfg in configs or candidates(M, N, K, dtype, tma_ok, beta=beta):
         r = time_config(sat, torch, M, N, K, dtype, cfg, dA, dB, dC, flush, runs, warmup, alpha, beta)
         r["tflops"] = 2.0 * M * N * K / (r["median_ms"] * 1e-3) / 1e12
         res.append(r)
@@ -85,17 +91,40 @@ def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None, alp
             "dispatcher": chosen}
 
 
-def write_table(entries, path=TABLE):
-    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits}}.",
+def table_row(e):
+    """The table line for one swept shape: its fastest configuration."""
+    best = min(e["results"], key=lambda r: r["median_ms"])
+    parts = best["config"].split(",")
+    bn, cg, raster, group = parts[:4]
+    nums = [p for p in parts[4:] if p.isdigit()]
+    splits = nums[0] if nums else "1"
+    cload = 1 if "cload" in parts[4:] else 0
+    return (f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}, "
+            f"{cload}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+
+
+def _key(line):
+    m = re.match(r"\{(-?\d+), (\d+), (\d+), (\d+),", line)
+    return tuple(int(x) for x in m.groups()) if m else None
+
+
+def write_table(entries, path=TABLE, merge=False):
+    """Write the winners as the dispatcher's table; with `merge`, rows of the
+    existing table for shapes not swept now are kept."""
+    rows = {}
+    if merge and os.path.exists(path):
+        with open(path) as f:
+            for line in f:
+                k = _key(line)
+                if k and k[0] >= 0:
+                    rows[k] = line.rstrip("\n")
+    for e in entries:
+        rows[(DT_CODE[e["dtype"]], e["M"], e["N"], e["K"])] = table_row(e)
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload}}.",
              "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
              "// (median of L2-flushed runs) of every candidate configuration."]
-    for e in entries:
-        best = min(e["results"], key=lambda r: r["median_ms"])
-        parts = best["config"].split(",")
-        bn, cg, raster, group = parts[:4]
-        splits = parts[4] if len(parts) > 4 and parts[4] != "plain" else "1"
-        lines.append(f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}}}}},"
-                     f"  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+    order = {1: 0, 2: 1, 0: 2}  # bf16, fp16, tf32
+    lines += [rows[k] for k in sorted(rows, key=lambda k: (order[k[0]], k[1:]))]
     lines.append("{-1, 0, 0, 0, {256, 1, 0, 8, 0}},")
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")
@@ -109,6 +138,7 @@ def main(argv=None):
     ap.add_argument("--configs", nargs="*", help="restrict to these configurations")
     ap.add_argument("--runs", type=int, default=30)
     ap.add_argument("--table", action="store_true", help="also write csrc/sweep_table.inc")
+    ap.add_argument("--merge", action="store_true", help="with --table: keep the rows of shapes not swept now")
     args = ap.parse_args(argv)
     sys.path.insert(0, os.path.dirname(HERE))
     import torch
@@ -136,7 +166,7 @@ def main(argv=None):
         with open(args.out, "w") as f:
             json.dump(entries, f, indent=1)
     if args.table:
-        write_table(entries)
+        write_table(entries, merge=args.merge)
 
 
 if __name__ == "__main__":

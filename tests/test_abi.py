@@ -54,7 +54,7 @@ def test_plan_create_fails_cleanly_without_a_gpu(lib):
 
 
 def _choice(M, N, K, dt, sms=152, tma=True):
-    bn, cg, raster, group, splits, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
+    bn, cg, raster, group, splits, cload, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
     return int(bn), int(cg), int(raster), int(group), int(splits), source
 
 
@@ -84,6 +84,22 @@ def test_dispatcher_splits_k_only_when_tiles_leave_sms_idle():
     assert _choice(256, 256, 16384, "bf16")[4] > 1
     assert _choice(4096, 4096, 4096, "bf16")[4] == 1
     assert _choice(8192, 8192, 8192, "tf32")[4] == 1
+
+
+def _cload(M, N, K, dt):
+    return int(sat.gemm_select_config(M, N, K, dt, 152, True).split(",")[5])
+
+
+def test_dispatcher_takes_c_through_the_ring_only_for_short_k():
+    # beta != 0: the ring measured faster where C is a large share of a tile's
+    # traffic (few k-blocks), slower behind a long K loop. Rule and table agree.
+    assert _cload(3000, 3000, 256, "bf16") == 0      # rule, 4 k-blocks
+    assert _cload(3000, 3000, 8192, "bf16") == 1     # rule, 128 k-blocks
+    assert _cload(3000, 3000, 1024, "tf32") == 0     # rule, 32 k-blocks
+    assert _cload(3000, 3000, 1056, "tf32") == 1     # rule, 33 k-blocks
+    assert _cload(4096, 4096, 512, "bf16") == 0      # table
+    assert _cload(16384, 1024, 4096, "bf16") == 1    # table
+    assert _cload(16384, 1024, 4096, "tf32") == 1    # table
 
 
 def test_dispatcher_rejects_bad_arguments():

@@ -20,8 +20,11 @@ from tests.gpu_util import run, run_np, stream, to_dev
 pytestmark = pytest.mark.gpu
 
 DTYPES = ["tf32", "bf16", "fp16"]
-# bn, cg, raster, group[, splits][, plain]
+# bn, cg, raster, group[, splits][, cload][, plain]. With beta != 0 the unsplit
+# TMA configurations other than 256,1 fetch C through the operand ring; ",cload"
+# makes the epilogue load C itself.
 CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,2,1,1",
+           "128,1,0,8,cload", "64,1,1,4,cload", "256,2,0,4,cload", "128,2,1,2,cload",
            "256,1,0,8,plain", "128,1,1,3,plain",
            "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain"]
 SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
@@ -76,6 +79,20 @@ def test_beta_zero_ignores_nan_c(dtype):
     _, ref32 = oracle.gemm(A, B, None, 2.0, 0.0, dtype)
     got, desc = run_np(M, N, K, dtype, A, B, None, 2.0, 0.0)   # C starts all NaN
     checks.assert_bit_exact(got, ref32, desc)
+
+
+@pytest.mark.parametrize("config", ["128,1,0,4", "256,2,0,2", "64,1,1,8"])
+def test_c_through_the_ring_many_tiles_per_cta(config):
+    """Several tiles per CTA walk the C stages round the ring: a tile takes
+    3 k-block stages plus 2 (bn 64, 128) or 4 (bn 256 pair) C stages, a
+    count prime to the ring's 6 or 8 stages, so C lands in every stage with
+    both parities of its fill barrier. M and N end in ragged tails."""
+    M, N, K = 6000, 3000, 136   # row strides 16-byte multiples: TMA; K tail of 8
+    A, B, C0 = si.problem(M, N, K, "bf16", "dyadic", 41, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, "bf16")
+    got, desc = run_np(M, N, K, "bf16", A, B, C0, 1.5, 0.5, config)
+    assert "cring" in desc
+    checks.assert_bit_exact(got, ref32, f"bf16 {M}x{N}x{K} [{desc}]")
 
 
 def test_k_zero_and_alpha_zero_scale_c():
