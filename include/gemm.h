@@ -56,7 +56,9 @@ typedef struct gemm_plan gemm_plan; /* opaque */
  * order, load path) for this problem on the CURRENT device, and prepare it.
  * M, N, K >= 0 and each < 2^31. Allocates host state and one 4-byte device
  * error word, both owned by the plan, and, when the choice splits K, a device
- * workspace of splits x ceil(M/256)*256 x N floats for the partial tiles.
+ * workspace of splits x ceil(M/256)*256 x N floats for the partial tiles;
+ * for a stream-K choice, one 128 x bn float partial tile and one counter
+ * per CTA of the grid (at most one per SM).
  * Returns NULL on failure; the reason is in gemm_last_error(). Must not be
  * called during CUDA stream capture.
  */
@@ -68,11 +70,15 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
  * where 2 needs bn >= 128; raster 0 = groups along M, 1 = along N;
  * group >= 1; splits 1..16 K splits, default 1), optionally followed by
  * ",cload" (with beta != 0 the epilogue loads C itself instead of the
- * producer fetching it through the operand ring) and ",plain" (force the
- * plain-load producer). NULL or "" means the dispatcher decides. For sweeps and tests; every configuration computes the same GEMM
- * (with splits > 1 the K sum is split into fixed slices whose partial tiles
- * are added in fixed order, so the bits can differ from splits = 1 but are
- * identical from run to run).
+ * producer fetching it through the operand ring), ",sk" (stream-K: the
+ * tiles of the last full wave and the partial one are cut into equal
+ * k-block ranges, one per CTA slot, and each split tile's pieces are added
+ * in fixed order) and ",plain" (force the plain-load producer). NULL or ""
+ * means the dispatcher decides. For sweeps and tests; every configuration
+ * computes the same GEMM (with splits > 1 or stream-K the K sum of some
+ * tiles is cut into fixed slices whose partial sums are added in fixed
+ * order, so the bits can differ from the unsplit order but are identical
+ * from run to run).
  */
 gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config);
 
@@ -90,9 +96,11 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
  * identical results. A plan that splits K launches a second kernel on the
  * same stream that sums the partial tiles in fixed order and applies alpha
  * and beta; its workspace is then in use until that kernel ends, so runs of
- * such a plan on different streams must be ordered by the caller. Other
- * plans are read-only here and may run on several streams or threads at
- * once. Launch failures return
+ * such a plan on different streams must be ordered by the caller. A
+ * stream-K plan's CTAs wait (bounded) for each other's partial tiles inside
+ * one launch, so it needs its whole grid resident: runs of such a plan must
+ * not overlap each other or other work that holds SMs for long. Other plans
+ * are read-only here and may run on several streams or threads at once. Launch failures return
  * GEMM_ERR_LAUNCH; kernel-side bounded-wait timeouts are reported by
  * gemm_plan_status().
  */
@@ -179,9 +187,10 @@ int gemm_selftest_bounded_wait(uint64_t timeout_ns);
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
  * strides are multiples of 16 bytes). Writes
- * "bn,cg,raster,group,splits,cload,source" (cload: 1 if, with beta != 0, the
- * epilogue loads C itself, 0 if the producer fetches it through the operand
- * ring where the kernel allows; source: rule or table) into `out`
+ * "bn,cg,raster,group,splits,cload,sk,source" (cload: 1 if, with beta != 0,
+ * the epilogue loads C itself, 0 if the producer fetches it through the
+ * operand ring where the kernel allows; sk: 1 for a stream-K schedule of the
+ * last waves; source: rule or table) into `out`
  * (NUL-terminated, at most `out_len` bytes). Returns 0, or GEMM_ERR_ARG on
  * bad arguments.
  */

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -107,6 +108,12 @@ struct gemm_plan {
     float* ws = nullptr;
     bool ws_tma = false;
     CUtensorMap tmW{};
+    // Stream-K (the choice's sk): layout, one 128 x BN partial tile and one
+    // counter per CTA, and the launch number the counters are compared with.
+    int sk_tiles = 0, sk_w = 0, sk_ctas = 0;
+    float* sk_ws = nullptr;
+    unsigned* sk_flags = nullptr;
+    mutable std::atomic<unsigned> sk_epoch{0};
     unsigned long long timeout_ns = 2000000000ull;
     char desc[256] = "";
     mutable std::mutex mu;
@@ -118,10 +125,9 @@ struct gemm_plan {
 
 namespace {
 
-int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
+// CTA slots (single CTAs, or pairs) that can be resident at once.
+int64_t slots_for(const gemm_plan* p, const sat::KernelEntry* e)
 {
-    const int64_t tm = 128 * e->cg;
-    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn) * p->splits;
     int64_t slots = p->sm_count / e->cg;
     if (e->cg == 2) {
         // Not every SM need be able to pair with a neighbour: ask the
@@ -130,8 +136,14 @@ int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
         if (n > 0 && n < slots)
             slots = n;
     }
-    if (slots < 1)
-        slots = 1;
+    return slots < 1 ? 1 : slots;
+}
+
+int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
+{
+    const int64_t tm = 128 * e->cg;
+    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn) * p->splits;
+    const int64_t slots = slots_for(p, e);
     return static_cast<int>((tiles < slots ? tiles : slots) * e->cg);
 }
 
@@ -183,26 +195,23 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     if (config && config[0]) {
         char head[64];
         std::snprintf(head, sizeof head, "%s", config);
-        // Optional tags after the numbers, in this order: ",cload" (the
-        // epilogue loads C itself), ",plain" (plain-load producer).
-        char* plain_tag = std::strstr(head, ",plain");
-        if (plain_tag) {
-            *plain_tag = '\0';
-            p->force_plain = true;
-        }
-        char* cload_tag = std::strstr(head, ",cload");
-        bool cload = false;
-        if (cload_tag) {
-            *cload_tag = '\0';
-            cload = true;
-        }
+        // Optional tags after the numbers, in any order: ",cload" (the
+        // epilogue loads C itself), ",sk" (stream-K), ",plain" (plain-load
+        // producer). Each is looked up first; the numbers end at the first.
+        char* tag[3] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain")};
+        const bool cload = tag[0] != nullptr, sk = tag[1] != nullptr;
+        p->force_plain = tag[2] != nullptr;
+        for (char* t : tag)
+            if (t)
+                *t = '\0';
         if (!sat::parse_choice(head, &p->choice)) {
-            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (want \"bn,cg,raster,group[,splits][,cload][,plain]\")",
-                 config);
+            fail(GEMM_ERR_ARG,
+                 "bad configuration \"%s\" (want \"bn,cg,raster,group[,splits][,cload][,sk][,plain]\")", config);
             delete p;
             return nullptr;
         }
         p->choice.cload = cload ? 1 : 0;
+        p->choice.sk = sk ? 1 : 0;
         source = "forced";
     } else {
         p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
@@ -259,12 +268,27 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
                 p->ws_tma = true;
         }
     }
+    // Stream-K (TMA path, unsplit): every slot runs, whatever the tile count.
+    if (e == cudaSuccess && c.sk && p->tma && p->splits == 1) {
+        const sat::KernelEntry* t = p->tma;
+        const int64_t tiles = ((M + 128 * t->cg - 1) / (128 * t->cg)) * ((N + t->bn - 1) / t->bn);
+        const int64_t slots = slots_for(p, t);
+        if (sat::sk_layout(tiles, num_kb, slots, &p->sk_tiles, &p->sk_w)) {
+            p->sk_ctas = static_cast<int>(slots * t->cg);
+            p->grid_tma = p->sk_ctas;
+            e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_ctas) * 128 * t->bn * sizeof(float));
+            if (e == cudaSuccess)
+                e = cudaMalloc(&p->sk_flags, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned));
+            if (e == cudaSuccess)
+                e = cudaMemset(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned));
+        }
+    }
     if (e != cudaSuccess) {
         cuda_fail(e, "allocating the device error word and workspace");
-        if (p->d_err)
-            cudaFree(p->d_err);
-        if (p->ws)
-            cudaFree(p->ws);
+        for (void* d : {static_cast<void*>(p->d_err), static_cast<void*>(p->ws), static_cast<void*>(p->sk_ws),
+                        static_cast<void*>(p->sk_flags)})
+            if (d)
+                cudaFree(d);
         delete p;
         return nullptr;
     }
@@ -274,11 +298,14 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
     const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
-    p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1;
-    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s",
+    p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1 && p->sk_tiles == 0;
+    char sk_desc[48] = "";
+    if (p->sk_tiles)
+        std::snprintf(sk_desc, sizeof sk_desc, " sk%d/%d", p->sk_tiles, p->sk_w);
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
                   p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
-                  source, p->c_ring ? " cring" : "");
+                  source, p->c_ring ? " cring" : "", sk_desc);
     return p;
 }
 
@@ -304,6 +331,10 @@ void gemm_plan_destroy(gemm_plan* plan)
         cudaFree(plan->d_err);
     if (plan->ws)
         cudaFree(plan->ws);
+    if (plan->sk_ws)
+        cudaFree(plan->sk_ws);
+    if (plan->sk_flags)
+        cudaFree(plan->sk_flags);
     delete plan;
 }
 
@@ -376,6 +407,24 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     const bool c_tma = split ? p->ws_tma : (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
+    if (use_tma && p->sk_tiles > 0) {
+        // Each launch has its own number; a slot's counter reaches number x
+        // (epilogue warps) once its partial tile of this launch is written.
+        // Before the counters could wrap, they are cleared and numbering restarts.
+        unsigned epoch = p->sk_epoch.fetch_add(1) + 1;
+        if (epoch >= (1u << 28)) {
+            e = cudaMemsetAsync(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned), stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "clearing the stream-K counters");
+            p->sk_epoch.store(1);
+            epoch = 1;
+        }
+        a.sk_tiles = p->sk_tiles;
+        a.sk_w = p->sk_w;
+        a.sk_ws = p->sk_ws;
+        a.sk_flags = p->sk_flags;
+        a.sk_epoch = epoch;
+    }
     CUtensorMap tmA{}, tmB{}, tmC{};
     if (split && c_tma) {
         tmC = p->tmW;
@@ -468,8 +517,13 @@ int gemm_plan_status(const gemm_plan* p)
         e = cudaMemset(p->d_err, 0, sizeof h);
     if (e != cudaSuccess)
         return cuda_fail(e, "reading the device error word");
-    if (h)
+    if (h) {
+        // A launch that gave up may have left stream-K counters short of its
+        // number: start the numbering again from cleared counters.
+        if (p->sk_flags && cudaMemset(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned)) == cudaSuccess)
+            p->sk_epoch.store(0);
         return fail(GEMM_ERR_TIMEOUT, "a bounded wait gave up inside the kernel (error bits 0x%x)", h);
+    }
     return GEMM_OK;
 }
 
@@ -504,8 +558,8 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
         return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
     const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
-    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
-                  c.splits > 1 ? c.splits : 1, c.cload, c.source == 1 ? "table" : "rule");
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.source == 1 ? "table" : "rule");
     return GEMM_OK;
 }
 

@@ -57,6 +57,22 @@ bool parse_choice(const char* spec, Choice* out)
     return true;
 }
 
+bool sk_layout(int64_t T, int64_t KB, int64_t G, int* sk_tiles, int* sk_w)
+{
+    if (KB < 1 || G < 2 || T <= G || T % G == 0)
+        return false;
+    // The partial wave alone, unless that would cut a tile into more than
+    // about five pieces; then the last full wave joins it.
+    int64_t sk = T % G;
+    if (cdiv(sk * KB, G) * 4 < KB)
+        sk += G;
+    if (sk * KB > 0x7fffffffLL)
+        return false;
+    *sk_tiles = static_cast<int>(sk);
+    *sk_w = static_cast<int>(cdiv(sk * KB, G));
+    return true;
+}
+
 Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool tma_ok)
 {
     for (const TableRow& r : kTable) {
@@ -133,6 +149,19 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
             if (ts < 0.8 * t1)
                 best.splits = s;
         }
+    }
+    // Stream-K when more than one wave of tiles ends in a partial one whose
+    // idle share is worth at least 3% of the run, and K is long enough for
+    // the fix-up of a split tile (one partial tile written and read per
+    // contributor) to be small against a tile's K loop.
+    if (best.splits == 1 && tma_ok) {
+        const int64_t tm = 128 * best.cg;
+        const int64_t tiles = cdiv(M, tm) * cdiv(N, best.bn);
+        const int64_t slots = std::max<int64_t>(1, sm_count / best.cg);
+        const int64_t kb = cdiv(K, dt == 0 ? 32 : 64);
+        const double f = static_cast<double>(tiles % slots) / static_cast<double>(slots);
+        const double idle = f > 0.0 ? (1.0 - f) / static_cast<double>(cdiv(tiles, slots)) : 0.0;
+        best.sk = tiles > slots && idle >= 0.03 && kb >= 32 ? 1 : 0;
     }
     return best;
 }

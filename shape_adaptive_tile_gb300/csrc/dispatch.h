@@ -13,7 +13,19 @@ struct Choice {
     int source;   // 0: analytic rule, 1: committed sweep table, 2: forced
     int splits;   // K splits (fixed-order reduction through a workspace); 0 or 1: none
     int cload;    // beta != 0: 1 = the epilogue loads C itself, 0 = the producer fetches it through the ring
+    int sk;       // 1: stream-K for the last waves of tiles (fixed-order fix-up of split tiles)
 };
+
+// Stream-K layout for T output tiles of KB k-blocks on G CTA slots: the
+// first *sk_tiles tiles (in raster order) are shared out as ranges of *sk_w
+// consecutive (tile, k-block) positions, one range per slot, which each
+// slot runs before its whole tiles. The shared tiles are those of the
+// partial last wave, or, where that would cut a tile into more than about
+// five pieces, those of the last full wave too. Returns false (no
+// stream-K) with at most one wave of tiles (measured slower there), when
+// the tiles fill whole waves exactly, or when the positions would not fit
+// an int.
+bool sk_layout(int64_t T, int64_t KB, int64_t G, int* sk_tiles, int* sk_w);
 
 // Picks tile and schedule. `tma_ok` says whether the TMA load path can be
 // used (16-byte-multiple row strides); when false only 1-SM tiles exist.

@@ -30,6 +30,16 @@ struct GemmArgs {
     int raster;                // 0: groups along M, 1: groups along N
     int c_tma;                 // 1: C is written (and read) through the TMA store path
     int c_ring;                // 1: the producer also fetches each tile's C (beta != 0) through the ring
+    // Stream-K (sk_tiles > 0; only with splits == 1): the first sk_tiles tiles
+    // in raster order are cut into k-block ranges of sk_w consecutive
+    // positions of the (tile, k-block) sequence, one range per CTA slot
+    // (CTA or CTA pair) g = 0 .. gridDim/cta_group - 1, taken before that
+    // slot's whole tiles sk_tiles + g, sk_tiles + g + slots, ...
+    int sk_tiles;
+    int sk_w;
+    float* sk_ws;              // per slot and CTA of a pair: 128 x BN fp32 partial tile
+    unsigned* sk_flags;        // per slot and CTA of a pair: epilogue warps done with the partial
+    unsigned sk_epoch;         // this launch's number (>= 1); a partial is ready at sk_epoch * epilogue warps
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;
 };

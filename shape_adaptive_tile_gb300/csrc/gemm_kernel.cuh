@@ -38,6 +38,7 @@ constexpr uint32_t kErrTimeoutProducer = 1u << 0;
 constexpr uint32_t kErrTimeoutMma = 1u << 1;
 constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDrain = 1u << 3;
+constexpr uint32_t kErrTimeoutPartial = 1u << 4;   // a stream-K partial tile never arrived
 
 template <int DT, int BN, int CG, int PROD>
 struct Traits {
@@ -136,8 +137,15 @@ __device__ __forceinline__ uint32_t swz_kmajor(int r, int k)
 // A work unit: output tile (tm, tn) of K split s, k-blocks [kb0, kb1).
 // Units of one split are consecutive, so CTAs running at the same time
 // share that split's K slice of the operands in L2.
+//
+// Stream-K pieces come in three kinds: a whole tile; a partial piece (it
+// does not start at k-block 0), whose raw sum goes to its slot's partial
+// tile; and a final piece (k-blocks 0 .. kb1 < num_kb), which adds the
+// partial pieces of slots g + 1 .. last, in that order, before the epilogue.
+constexpr int kWhole = 0, kSkPartial = 1, kSkFinal = 2;
+
 struct Unit {
-    int tm, tn, s, kb0, kb1;
+    int tm, tn, s, kb0, kb1, kind, last;
 };
 
 __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
@@ -148,7 +156,49 @@ __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
     tile_coord(u - w.s * per, a, w.tm, w.tn);
     w.kb0 = w.s * a.kb_per_split;
     w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
+    w.kind = kWhole;
+    w.last = 0;
     return w;
+}
+
+// The sequence of units of CTA slot g out of G: its stream-K range of
+// (tile, k-block) positions [pos, end), cut at tile boundaries, then its
+// whole units t = sk_tiles + g, sk_tiles + g + G, ... Without stream-K
+// this is t = g, g + G, ...
+struct WorkIter {
+    int pos, end, t;
+};
+
+__device__ __forceinline__ WorkIter work_begin(const GemmArgs& a, int g)
+{
+    WorkIter it;
+    const int total = a.sk_tiles * a.num_kb;
+    it.pos = a.sk_tiles > 0 ? min(g * a.sk_w, total) : 0;
+    it.end = a.sk_tiles > 0 ? min(it.pos + a.sk_w, total) : 0;
+    it.t = a.sk_tiles + g;
+    return it;
+}
+
+template <bool kSK = true>
+__device__ __forceinline__ bool work_next(const GemmArgs& a, int G, WorkIter& it, Unit& w)
+{
+    if (kSK && it.pos < it.end) {
+        const int tile = it.pos / a.num_kb;
+        tile_coord(tile, a, w.tm, w.tn);
+        w.s = 0;
+        w.kb0 = it.pos - tile * a.num_kb;
+        w.kb1 = min(a.num_kb, w.kb0 + (it.end - it.pos));
+        w.kind = w.kb0 > 0 ? kSkPartial : (w.kb1 < a.num_kb ? kSkFinal : kWhole);
+        w.last = (tile * a.num_kb + a.num_kb - 1) / a.sk_w;
+        it.pos += w.kb1 - w.kb0;
+        return true;
+    }
+    if (it.t < a.num_tiles) {
+        w = unit_coord(it.t, a);
+        it.t += G;
+        return true;
+    }
+    return false;
 }
 
 // Byte offset of B element (k, n) in the MN-major tile: column blocks of
@@ -203,27 +253,30 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         return j < AS ? sA + static_cast<uint32_t>(s * T::A_BYTES + j * 4096)
                       : sB + static_cast<uint32_t>(s * T::B_BYTES + (j - AS) * 4096);
     };
-    const bool c_ring = T::C_RING_OK && args.c_ring != 0 && args.c_tma != 0 && args.splits == 1 && args.beta != 0.0f;
+    const bool c_ring = T::C_RING_OK && args.c_ring != 0 && args.c_tma != 0 && args.splits == 1 && args.sk_tiles == 0 &&
+                        args.beta != 0.0f;
 
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < T::STAGES; ++s) {
-            mbar_init(full_bar(s), PROD == kProdTMA ? 1 : T::NPW * 32);
-            mbar_init(empty_bar(s), 1);
+    // Barrier initialisation, spread over the lanes of warp 0: lane s < STAGES
+    // takes ring stage s, the next two lanes the accumulator barriers, the
+    // next one the rest.
+    static_assert(T::STAGES + 3 <= 32, "one lane per stage");
+    if (warp == 0) {
+        if (lane < T::STAGES) {
+            mbar_init(full_bar(lane), PROD == kProdTMA ? 1 : T::NPW * 32);
+            mbar_init(empty_bar(lane), 1);
+            mbar_init(cfull_bar(lane), 1);
+            c_readers[lane] = 0;
+        } else if (lane < T::STAGES + 2) {
+            mbar_init(tfull_bar(lane - T::STAGES), 1);
+            mbar_init(tempty_bar(lane - T::STAGES), T::EPI_WARPS * CG);
+        } else if (lane == T::STAGES + 2) {
+            mbar_init(drain_bar, 1);
+            mbar_init(tmem_ready_bar, 1);
+            *abort_flag = 0;
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), T::EPI_WARPS * CG);
-        }
-        for (int s = 0; s < T::STAGES; ++s) {
-            mbar_init(cfull_bar(s), 1);
-            c_readers[s] = 0;
-        }
-        mbar_init(drain_bar, 1);
-        mbar_init(tmem_ready_bar, 1);
-        *abort_flag = 0;
         fence_mbar_init();
     }
     if (PROD == kProdTMA && warp == 0 && lane == 0) {
@@ -271,8 +324,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 bool ok = true;
                 // The pair's loads all complete on the leader's barrier.
                 const uint32_t full0 = CG == 2 ? map_to_cta(full_bar(0), 0) : full_bar(0);
-                for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                    const Unit w = unit_coord(t, args);
+                WorkIter it = work_begin(args, tile0);
+                Unit w;
+                while (ok && work_next(args, tile_step, it, w)) {
                     const int m0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
                     const int n0 = w.tn * BN + static_cast<int>(rank) * T::BN_CTA;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -368,8 +422,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int fills = 0, signalled = 0;
-            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                const Unit w = unit_coord(t, args);
+            WorkIter it = work_begin(args, tile0);
+            Unit w;
+            while (ok && work_next(args, tile_step, it, w)) {
                 const int m0 = w.tm * T::BM;
                 const int n0 = w.tn * BN;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -445,8 +500,9 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                const Unit w = unit_coord(t, args);
+            WorkIter it = work_begin(args, tile0);
+            Unit w;
+            while (ok && work_next(args, tile_step, it, w)) {
                 const int m0 = w.tm * T::BM;
                 const int n0 = w.tn * BN;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -529,14 +585,15 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             bool ok = true, issued = false;
             if constexpr (CG == 2)
                 ok = wait_bar<true>(tmem_ready_bar, 0, wc, kErrTimeoutMma);
-            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
+            WorkIter it = work_begin(args, tile0);
+            Unit w;
+            while (ok && work_next(args, tile_step, it, w)) {
                 if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {  // peer epilogue releases: cluster scope
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
-                const Unit w = unit_coord(t, args);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar<false>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma)) {
                         ok = false;
@@ -624,16 +681,26 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         // The tile loop, compiled twice: with C through the ring, and with C
         // loaded by the epilogue (or not read), so that each copy keeps only
         // the registers its own path needs.
-        auto tile_loop = [&](auto ring_tag) {
-            constexpr bool RING = decltype(ring_tag)::value;
-            const bool prefetch_c = !RING && args.c_tma && beta != 0.0f;   // beta != 0 only unsplit
+        WorkIter it = work_begin(args, tile0);
+        bool ok = true;
+        auto tile_loop = [&](auto mode_tag) {
+            constexpr int MODE = decltype(mode_tag)::value;
+            constexpr bool RING = MODE == 1;  // C through the operand ring
+            constexpr bool SK = MODE == 2;    // stream-K pieces
+            // beta != 0 (only unsplit): the plain copy reads each chunk's C
+            // ahead (the first one before the accumulator wait); the
+            // stream-K copy reads it only when the chunk is stored, after any
+            // partial sums have been added, to keep its registers in bounds.
+            const bool prefetch_c = MODE == 0 && args.c_tma && beta != 0.0f;
+            const bool late_c = SK && args.c_tma && beta != 0.0f;
             // C through the ring: where the next unit's stages start, and per
             // stage the parity of its next C fill.
             int rpos = 0;
             uint32_t cpar = 0;
-            bool ok = true;
-            for (int t = tile0; ok && t < args.num_tiles; t += tile_step) {
-                const Unit w = unit_coord(t, args);
+            Unit w;
+            // The stream-K copy takes this CTA's stream-K pieces; the others
+            // take whole units (all of them, or those after the pieces).
+            while (ok && (SK ? it.pos < it.end : true) && work_next<SK>(args, tile_step, it, w)) {
                 const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
                 const int n0 = w.tn * BN;
                 int cst = 0;  // ring stage holding this tile's first C chunks
@@ -651,6 +718,22 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
                     break;
                 tc_fence_after();
+                if constexpr (SK) {
+                    // Stream-K final piece: the partial tiles of slots
+                    // tile0 + 1 .. w.last (same rows of the same tile) must
+                    // have been written before they are added below.
+                    if (w.kind == kSkFinal) {
+                        if (lane == 0) {
+                            for (int j = tile0 + 1; ok && j <= w.last; ++j)
+                                ok = wait_counter(args.sk_flags + j * CG + static_cast<int>(rank),
+                                                  args.sk_epoch * static_cast<unsigned>(T::EPI_WARPS), wc,
+                                                  kErrTimeoutPartial);
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok)
+                            break;
+                    }
+                }
                 // Split s writes its slice of the output: rows s * out_rows + row.
                 const int yoff = w.s * args.out_rows;
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
@@ -672,6 +755,38 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         }
                     }
                     const int gcol0 = n0 + c * 32;
+                    if constexpr (SK) {
+                        // Partial tile of slot g, as [column chunk][16-byte
+                        // piece q][row]: lane-consecutive 16-byte pieces, so
+                        // both the writer and the reader move whole lines.
+                        if (w.kind != kWhole) {
+                            const int row = sub * 32 + lane;
+                            if (w.kind == kSkPartial) {
+                                float* slot = args.sk_ws + static_cast<int64_t>(tile0 * CG + static_cast<int>(rank)) * (128 * BN);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    st_global_v4(slot + ((c * 8 + q) * 128 + row) * 4, __uint_as_float(r[4 * q]),
+                                                 __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                                 __uint_as_float(r[4 * q + 3]));
+                                continue;
+                            }
+                            // Final piece: add the later slots' partial sums,
+                            // in ascending slot order.
+#pragma unroll 1
+                            for (int j = tile0 + 1; j <= w.last; ++j) {
+                                const float* slot =
+                                    args.sk_ws + static_cast<int64_t>(j * CG + static_cast<int>(rank)) * (128 * BN);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    float p[4];
+                                    ld_global_cg_v4(slot + ((c * 8 + q) * 128 + row) * 4, p[0], p[1], p[2], p[3]);
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        r[4 * q + e] = __float_as_uint(__uint_as_float(r[4 * q + e]) + p[e]);
+                                }
+                            }
+                        }
+                    }
                     if (args.c_tma) {
                         // Bulk-store path: this thread owns row (row0 + lane) of the
                         // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
@@ -693,7 +808,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                                 break;
                             }
                             csrc = ring_slot(cst_c, id - cs * T::CPS) + static_cast<uint32_t>(lane * 128);
-                        } else if (prefetch_c && c != half) {
+                        } else if ((prefetch_c && c != half) || late_c) {
                             load_c(cv, grow, gcol0);
                         }
                         if (lane == 0)
@@ -764,19 +879,34 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 if constexpr (RING) {
                     for (int cs = 0; cs < T::NCS; ++cs)
                         cpar ^= 1u << (cst + cs < T::STAGES ? cst + cs : cst + cs - T::STAGES);
+                } else if constexpr (SK) {
+                    if (w.kind == kSkPartial) {
+                        // Publish this warp's share of the partial tile.
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0)
+                            red_release_add(args.sk_flags + tile0 * CG + static_cast<int>(rank), 1u);
+                    }
                 }
                 acc ^= 1;
                 if (acc == 0)
                     acc_phase ^= 1u;
             }
         };
-        if constexpr (T::C_RING_OK) {
-            if (c_ring)
-                tile_loop(std::true_type{});
-            else
-                tile_loop(std::false_type{});
+        using Plain = std::integral_constant<int, 0>;
+        using Ring = std::integral_constant<int, 1>;
+        using StreamK = std::integral_constant<int, 2>;
+        if (PROD == kProdTMA && args.sk_tiles > 0) {
+            // Stream-K pieces first, then the whole tiles in the plain copy
+            // (the pieces' extra work does not weigh on its registers).
+            if constexpr (PROD == kProdTMA)
+                tile_loop(StreamK{});
+            tile_loop(Plain{});
+        } else if (T::C_RING_OK && c_ring) {
+            if constexpr (T::C_RING_OK)
+                tile_loop(Ring{});
         } else {
-            tile_loop(std::false_type{});
+            tile_loop(Plain{});
         }
         if (args.c_tma && lane == 0)
             bulk_wait<0>();  // every bulk store of this warp has completed

@@ -25,9 +25,11 @@
 
 namespace {
 
-// 16 MiB: 256 bytes for the status word, the rest for split-K partial tiles.
-constexpr size_t kScratchBytes = size_t(16) << 20;
-constexpr size_t kStatusBytes = 256;
+// 32 MiB: 4 KiB for the status word (offset 0) and the stream-K counters
+// (offset 256, one per CTA), the rest for split-K or stream-K partial tiles.
+constexpr size_t kScratchBytes = size_t(32) << 20;
+constexpr size_t kStatusBytes = 4096;
+constexpr size_t kCounterOffset = 256;
 constexpr size_t kWorkspaceBytes = kScratchBytes - kStatusBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -122,18 +124,23 @@ int setup_device(int dev, DeviceState** out)
     return GEMM_OK;
 }
 
-int grid_for(int64_t M, int64_t N, int splits, int sm_count, const sat::KernelEntry* e)
+// CTA slots (single CTAs, or pairs) that can be resident at once.
+int64_t slots_for(int sm_count, const sat::KernelEntry* e)
 {
-    const int64_t tm = 128 * e->cg;
-    const int64_t units = ((M + tm - 1) / tm) * ((N + e->bn - 1) / e->bn) * splits;
     int64_t slots = sm_count / e->cg;
     if (e->cg == 2) {
         const int n = e->max_clusters();
         if (n > 0 && n < slots)
             slots = n;
     }
-    if (slots < 1)
-        slots = 1;
+    return slots < 1 ? 1 : slots;
+}
+
+int grid_for(int64_t M, int64_t N, int splits, int sm_count, const sat::KernelEntry* e)
+{
+    const int64_t tm = 128 * e->cg;
+    const int64_t units = ((M + tm - 1) / tm) * ((N + e->bn - 1) / e->bn) * splits;
+    const int64_t slots = slots_for(sm_count, e);
     return static_cast<int>((units < slots ? units : slots) * e->cg);
 }
 
@@ -196,14 +203,31 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
                     "this problem splits K %d ways and needs %zu bytes of scratch; the allocation-free entry point "
                     "has %zu bytes (use gemm_plan_create/gemm_run, which allocate their own workspace)",
                     splits, ws_bytes, kWorkspaceBytes);
+    // Stream-K, laid out as gemm_plan_create lays it out.
+    int sk_tiles = 0, sk_w = 0;
+    int64_t sk_ctas = 0;
+    if (c.sk && use_tma && splits == 1) {
+        const int64_t tiles = ((M + tile_rows - 1) / tile_rows) * ((N + k->bn - 1) / k->bn);
+        const int64_t slots = slots_for(ds->sm_count, k);
+        if (sat::sk_layout(tiles, num_kb, slots, &sk_tiles, &sk_w)) {
+            sk_ctas = slots * k->cg;
+            const size_t need = static_cast<size_t>(sk_ctas) * 128 * k->bn * 4;
+            if (need > kWorkspaceBytes || kCounterOffset + static_cast<size_t>(sk_ctas) * 4 > kStatusBytes)
+                return fail(GEMM_ERR_ARG,
+                            "this problem's stream-K partial tiles need %zu bytes of scratch; the allocation-free "
+                            "entry point has %zu bytes (use gemm_plan_create/gemm_run)",
+                            need, kWorkspaceBytes);
+        }
+    }
     e = k->prepare();
     if (e != cudaSuccess)
         return fail(GEMM_ERR_LAUNCH, "setting the kernel's shared-memory limit: %s", cudaGetErrorString(e));
 
     uint32_t* status = static_cast<uint32_t*>(ds->scratch);
     float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(ds->scratch) + kStatusBytes);
-    // The array keeps the previous call's contents; the status word must start at zero.
-    e = cudaMemsetAsync(status, 0, sizeof(uint32_t), stream);
+    // The array keeps the previous call's contents; the status word and the
+    // stream-K counters must start at zero (this call is launch number 1).
+    e = cudaMemsetAsync(status, 0, kStatusBytes, stream);
     if (e != cudaSuccess)
         return fail(GEMM_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
 
@@ -238,14 +262,22 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
                          CU_TENSOR_MAP_SWIZZLE_128B))
         return fail(GEMM_ERR_LAUNCH, "encoding the output tensor map");
     a.c_tma = c_tma ? 1 : 0;
-    a.c_ring = !c.cload && use_tma && k->c_ring && c_tma && splits == 1 && beta != 0.0f ? 1 : 0;
+    a.c_ring = !c.cload && use_tma && k->c_ring && c_tma && splits == 1 && sk_tiles == 0 && beta != 0.0f ? 1 : 0;
+    if (sk_tiles > 0) {
+        a.sk_tiles = sk_tiles;
+        a.sk_w = sk_w;
+        a.sk_ws = ws;
+        a.sk_flags = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(ds->scratch) + kCounterOffset);
+        a.sk_epoch = 1;
+    }
     if (use_tma) {
         if (!encode(&tmA, tdt, es, A, K, M, static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tmB, tdt, es, B, N, K, static_cast<uint32_t>(128 / es), static_cast<uint32_t>(k->bk),
                     static_cast<CUtensorMapSwizzle>(k->b_swizzle)))
             return fail(GEMM_ERR_LAUNCH, "encoding the operand tensor maps");
     }
-    e = k->launch(&tmA, &tmB, &tmC, &a, grid_for(M, N, splits, ds->sm_count, k), stream);
+    e = k->launch(&tmA, &tmB, &tmC, &a, sk_tiles > 0 ? static_cast<int>(sk_ctas) : grid_for(M, N, splits, ds->sm_count, k),
+                  stream);
     if (e != cudaSuccess)
         return fail(GEMM_ERR_LAUNCH, "launching the GEMM kernel: %s", cudaGetErrorString(e));
     if (splits > 1) {

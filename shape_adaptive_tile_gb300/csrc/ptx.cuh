@@ -148,6 +148,45 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     return wait_slow<kCluster>(bar, parity, w, code);
 }
 
+// Bounded wait until the global counter *f reaches `target` (acquire at GPU
+// scope, so what the counting CTA wrote before its release is visible).
+static __device__ __noinline__ bool wait_counter(const unsigned* f, unsigned target, const WaitCtl& w, uint32_t code)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+        if (v >= target)
+            return true;
+        if (*w.abort)
+            return false;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            *w.abort = 1;
+            if (w.err)
+                atomicOr(w.err, code);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+// *f += v with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_add(unsigned* f, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(float* p, float a, float b, float c, float d)
+{
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// 16-byte global load cached in L2 only (data written by other CTAs).
+__device__ __forceinline__ void ld_global_cg_v4(const float* p, float& a, float& b, float& c, float& d)
+{
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "l"(p) : "memory");
+}
+
 // ---- proxies -----------------------------------------------------------------
 
 // Make this thread's generic-proxy shared-memory view visible to the async

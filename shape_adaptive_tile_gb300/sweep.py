@@ -37,8 +37,13 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
     for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
         if not tma_ok and (cg == 2 or bn == 64):
             continue
+        tiles = -(-M // (128 * cg)) * -(-N // bn)
+        slots = sm_count // cg
         for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
             out.append(f"{bn},{cg},{raster},{group}")
+            # stream-K where more than a wave of tiles ends in a partial one
+            if tma_ok and tiles > slots and tiles % slots:
+                out.append(f"{bn},{cg},{raster},{group},sk")
             # beta != 0: also with the epilogue loading C itself instead of
             # the producer fetching it through the ring (the 1-SM 256-wide
             # tile has no ring stages to spare, so it always loads C itself)
@@ -99,8 +104,9 @@ def table_row(e):
     nums = [p for p in parts[4:] if p.isdigit()]
     splits = nums[0] if nums else "1"
     cload = 1 if "cload" in parts[4:] else 0
+    sk = 1 if "sk" in parts[4:] else 0
     return (f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}, "
-            f"{cload}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+            f"{cload}, {sk}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
 
 
 def _key(line):
@@ -120,7 +126,7 @@ def write_table(entries, path=TABLE, merge=False):
                     rows[k] = line.rstrip("\n")
     for e in entries:
         rows[(DT_CODE[e["dtype"]], e["M"], e["N"], e["K"])] = table_row(e)
-    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload}}.",
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload, sk}}.",
              "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
              "// (median of L2-flushed runs) of every candidate configuration."]
     order = {1: 0, 2: 1, 0: 2}  # bf16, fp16, tf32

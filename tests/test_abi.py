@@ -54,7 +54,7 @@ def test_plan_create_fails_cleanly_without_a_gpu(lib):
 
 
 def _choice(M, N, K, dt, sms=152, tma=True):
-    bn, cg, raster, group, splits, cload, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
+    bn, cg, raster, group, splits, cload, sk, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
     return int(bn), int(cg), int(raster), int(group), int(splits), source
 
 
@@ -98,8 +98,22 @@ def test_dispatcher_takes_c_through_the_ring_only_for_short_k():
     assert _cload(3000, 3000, 1024, "tf32") == 0     # rule, 32 k-blocks
     assert _cload(3000, 3000, 1056, "tf32") == 1     # rule, 33 k-blocks
     assert _cload(4096, 4096, 512, "bf16") == 0      # table
-    assert _cload(16384, 1024, 4096, "bf16") == 1    # table
-    assert _cload(16384, 1024, 4096, "tf32") == 1    # table
+    # table: the long-K shape loads C in the epilogue (stream-K runs do too)
+    for dt in ("bf16", "tf32"):
+        f = sat.gemm_select_config(16384, 1024, 4096, dt, 152, True).split(",")
+        assert f[5] == "1" or f[6] == "1"
+
+
+def _sk(M, N, K, dt, sms=152):
+    return int(sat.gemm_select_config(M, N, K, dt, sms, True).split(",")[6])
+
+
+def test_dispatcher_stream_k_only_past_one_wave_with_a_partial_last_one():
+    assert _sk(6144, 6144, 4096, "bf16") == 1    # 576 pair tiles: 7 waves of 76 plus 44
+    assert _sk(5000, 5000, 5000, "tf32") == 1
+    assert _sk(2000, 2000, 4096, "bf16") == 0    # 64 pair tiles: less than one wave
+    assert _sk(4864, 19456, 4096, "bf16") == 0   # 19 x 76 pair tiles: whole waves
+    assert _sk(3000, 3000, 128, "bf16") == 0     # K too short for the fix-up to pay
 
 
 def test_dispatcher_rejects_bad_arguments():

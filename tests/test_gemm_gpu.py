@@ -23,10 +23,13 @@ DTYPES = ["tf32", "bf16", "fp16"]
 # bn, cg, raster, group[, splits][, cload][, plain]. With beta != 0 the unsplit
 # TMA configurations other than 256,1 fetch C through the operand ring; ",cload"
 # makes the epilogue load C itself.
+# ",sk" (stream-K) asked for where there is at most one wave of tiles: the
+# plan runs whole tiles only.
 CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,2,1,1",
            "128,1,0,8,cload", "64,1,1,4,cload", "256,2,0,4,cload", "128,2,1,2,cload",
            "256,1,0,8,plain", "128,1,1,3,plain",
-           "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain"]
+           "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain",
+           "256,2,0,4,sk", "128,1,0,8,sk", "64,1,1,4,sk"]
 SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
 
 
@@ -93,6 +96,61 @@ def test_c_through_the_ring_many_tiles_per_cta(config):
     got, desc = run_np(M, N, K, "bf16", A, B, C0, 1.5, 0.5, config)
     assert "cring" in desc
     checks.assert_bit_exact(got, ref32, f"bf16 {M}x{N}x{K} [{desc}]")
+
+
+# Stream-K: 1650 x 3192 makes 325 tiles of 128 x 128 (2 waves of 152 plus
+# 21), 91 CTA-pair tiles of 256 x 256 (76 plus 15) and 650 tiles of 128 x 64
+# (4 x 152 plus 42). With K = 632/636 the first two share out the last full
+# wave and the partial one (the partial wave alone would cut a tile into too
+# many pieces), the third only the partial wave.
+@pytest.mark.parametrize("config", ["128,1,0,4,sk", "256,2,0,4,sk", "64,1,1,8,sk"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_stream_k_waves_dyadic_exact(dtype, config):
+    M, N, K = 1650, 3192, 632 if dtype == "bf16" else 636
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 51, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+    assert " sk" in desc
+    checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+@pytest.mark.parametrize("config", ["256,2,0,4,sk", "128,1,0,4,sk", "64,1,1,8,sk"])
+def test_stream_k_is_deterministic_and_within_tolerance(config):
+    """Gaussian inputs: the split tiles' partial sums are added in a fixed
+    order, so five runs give the same bits, within the dtype's bound."""
+    M, N, K = 1650, 3192, 2048
+    A, B, C0 = si.problem(M, N, K, "tf32", "normal", 52, "normal")
+    ref64, _ = oracle.gemm(A, B, C0, 1.0, 1.0, "tf32")
+    dA, dB = to_dev(A, "tf32"), to_dev(B, "tf32")
+    out = torch.empty(M, N, device="cuda")
+    first = None
+    with sat.Plan(M, N, K, "tf32", config) as plan:
+        desc = plan.describe()
+        assert " sk" in desc
+        for i in range(5):
+            out.copy_(to_dev(C0))
+            run(plan, dA, dB, out, 1.0, 1.0)
+            bits = out.view(torch.int32).clone()
+            if first is None:
+                first = bits
+            else:
+                assert torch.equal(bits, first), f"run {i} differs [{desc}]"
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    checks.assert_rel_rms(first.view(torch.float32).cpu().numpy(), ref64, si.REL_RMS_BOUND["tf32"], desc)
+
+
+def test_stream_k_with_c_not_16_byte_aligned():
+    M, N, K = 2000, 1400, 512   # 176 tiles of 128 x 128: the partial wave of 24 is shared out
+    A, B, C0 = si.problem(M, N, K, "bf16", "dyadic", 53, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, "bf16")
+    flatC = to_dev(np.concatenate([np.zeros(1, np.float32), C0.ravel()]))
+    with sat.Plan(M, N, K, "bf16", "128,1,0,4,sk") as plan:
+        assert " sk" in plan.describe()
+        run(plan, to_dev(A, "bf16"), to_dev(B, "bf16"), flatC.data_ptr() + 4, 1.5, -0.5)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    checks.assert_bit_exact(flatC[1:].view(M, N).cpu().numpy(), ref32, "stream-K, C misaligned")
 
 
 def test_k_zero_and_alpha_zero_scale_c():

@@ -29,6 +29,7 @@ CASES = [
     ("tf32", 300, 260, 200, "normal", 1.0, 0.0),     # no split: only the status word is scratch
     ("fp16", 513, 264, 130, "dyadic", 1.0, 1.0),
     ("bf16", 333, 517, 389, "uniform", 1.5, 0.5),    # misaligned row strides: plain-load producer
+    ("bf16", 6144, 6144, 4096, "normal", 1.0, 0.0),  # stream-K: partial tiles and counters in the scratch
 ]
 
 
@@ -69,7 +70,7 @@ def test_noalloc_matches_gemm_run_on_two_calls(case):
 
 def _split_workspace_bytes(M, N, K, dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    bn, cg, _, _, splits, _, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
+    bn, cg, _, _, splits, _, _, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
     rows = 128 * int(cg)
     return int(splits), int(splits) * (-(-M // rows) * rows) * N * 4
 
@@ -77,23 +78,19 @@ def _split_workspace_bytes(M, N, K, dtype):
 @pytest.mark.parametrize("dtype,M,N,K", [("bf16", 256, 4096, 8192), ("tf32", 128, 2048, 16384)])
 def test_noalloc_cases_really_split_k_within_the_scratch(dtype, M, N, K):
     splits, ws = _split_workspace_bytes(M, N, K, dtype)
-    assert splits > 1 and ws <= (16 << 20) - 256
+    assert splits > 1 and ws <= (32 << 20) - 4096
 
 
-# bf16 128 x 19456 x 8192 splits K 2 ways (19 MiB of partial tiles); the
-# benchmark's bf16 128 x 8192 x 8192 splits 4 ways (16 MiB): both exceed the
-# 16 MiB - 256 bytes of workspace.
-@pytest.mark.parametrize("M,N,K", [(128, 19456, 8192), (128, 8192, 8192)])
-def test_noalloc_rejects_a_problem_beyond_its_scratch(M, N, K):
-    splits, ws = _split_workspace_bytes(M, N, K, "bf16")
-    if splits < 2 or ws <= (16 << 20) - 256:
-        pytest.skip(f"the dispatcher does not need more scratch than the array holds here ({splits}, {ws})")
-    x = torch.zeros(64, dtype=torch.bfloat16, device="cuda")   # never read: rejected before any launch
-    c = torch.zeros(64, device="cuda")
-    rc = sat.gemm_run_noalloc(M, N, K, "bf16", x, x, c, 1.0, 0.0, stream())
-    assert rc == -1
-    assert "scratch" in sat.gemm_last_error()
-    # and the entry point still works afterwards
+def test_noalloc_case_really_uses_stream_k():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sat.gemm_select_config(6144, 6144, 4096, "bf16", sms, True).split(",")[6] == "1"
+
+
+def test_noalloc_works_after_a_rejected_call():
+    # A bad call (here a NULL operand) is rejected before any launch, and
+    # the entry point still works afterwards.
+    c = torch.zeros(64 * 64, device="cuda")
+    assert sat.gemm_run_noalloc(64, 64, 64, "bf16", None, None, c, 1.0, 0.0, stream()) == -1
     A, B, _ = si.problem(64, 64, 64, "bf16", "dyadic", 3)
     out = torch.empty(64, 64, device="cuda")
     assert sat.gemm_run_noalloc(64, 64, 64, "bf16", to_dev(A, "bf16"), to_dev(B, "bf16"), out, 1.0, 0.0,
