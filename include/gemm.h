@@ -70,7 +70,9 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
  * where 2 needs bn >= 128; raster 0 = groups along M, 1 = along N;
  * group >= 1; splits 1..16 K splits, default 1), optionally followed by
  * ",cload" (with beta != 0 the epilogue loads C itself instead of the
- * producer fetching it through the operand ring), ",sk" (stream-K: the
+ * producer fetching it through the operand ring), ",swap" (operand roles
+ * exchanged: the tensor core computes C^T = B^T A^T in tiles of 128 columns
+ * by bn rows of C; cg 1, bn 64 or 128), ",sk" (stream-K: the
  * tiles of the last full wave and the partial one are cut into equal
  * k-block ranges, one per CTA slot, and each split tile's pieces are added
  * in fixed order) and ",plain" (force the plain-load producer). NULL or ""
@@ -187,10 +189,11 @@ int gemm_selftest_bounded_wait(uint64_t timeout_ns);
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
  * strides are multiples of 16 bytes). Writes
- * "bn,cg,raster,group,splits,cload,sk,source" (cload: 1 if, with beta != 0,
- * the epilogue loads C itself, 0 if the producer fetches it through the
- * operand ring where the kernel allows; sk: 1 for a stream-K schedule of the
- * last waves; source: rule or table) into `out`
+ * "bn,cg,raster,group,splits,cload,sk,swap,source" (cload: 1 if, with
+ * beta != 0, the epilogue loads C itself, 0 if the producer fetches it
+ * through the operand ring where the kernel allows; sk: 1 for a stream-K
+ * schedule of the last waves; swap: 1 if the tensor core computes C^T =
+ * B^T A^T, with bn rows of C per tile; source: rule or table) into `out`
  * (NUL-terminated, at most `out_len` bytes). Returns 0, or GEMM_ERR_ARG on
  * bad arguments.
  */

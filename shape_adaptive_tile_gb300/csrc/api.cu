@@ -141,8 +141,9 @@ int64_t slots_for(const gemm_plan* p, const sat::KernelEntry* e)
 
 int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
 {
-    const int64_t tm = 128 * e->cg;
-    const int64_t tiles = ((p->M + tm - 1) / tm) * ((p->N + e->bn - 1) / e->bn) * p->splits;
+    int64_t tm = 0, tn = 0;
+    sat::tile_grid(e, p->M, p->N, &tm, &tn);
+    const int64_t tiles = tm * tn * p->splits;
     const int64_t slots = slots_for(p, e);
     return static_cast<int>((tiles < slots ? tiles : slots) * e->cg);
 }
@@ -198,20 +199,28 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         // Optional tags after the numbers, in any order: ",cload" (the
         // epilogue loads C itself), ",sk" (stream-K), ",plain" (plain-load
         // producer). Each is looked up first; the numbers end at the first.
-        char* tag[3] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain")};
-        const bool cload = tag[0] != nullptr, sk = tag[1] != nullptr;
+        char* tag[4] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain"),
+                        std::strstr(head, ",swap")};
+        const bool cload = tag[0] != nullptr, sk = tag[1] != nullptr, swap = tag[3] != nullptr;
         p->force_plain = tag[2] != nullptr;
         for (char* t : tag)
             if (t)
                 *t = '\0';
         if (!sat::parse_choice(head, &p->choice)) {
             fail(GEMM_ERR_ARG,
-                 "bad configuration \"%s\" (want \"bn,cg,raster,group[,splits][,cload][,sk][,plain]\")", config);
+                 "bad configuration \"%s\" (want \"bn,cg,raster,group[,splits][,cload][,sk][,swap][,plain]\")",
+                 config);
             delete p;
             return nullptr;
         }
         p->choice.cload = cload ? 1 : 0;
         p->choice.sk = sk ? 1 : 0;
+        p->choice.swap = swap ? 1 : 0;
+        if (swap && (p->choice.cg != 1 || p->choice.bn == 256)) {
+            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (a swapped tile is 1-SM with bn 32, 64 or 128)", config);
+            delete p;
+            return nullptr;
+        }
         source = "forced";
     } else {
         p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
@@ -219,7 +228,7 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     }
     const sat::Choice& c = p->choice;
     if (tma_ok && !p->force_plain) {
-        p->tma = sat::find_entry(dt, c.bn, c.cg, sat::kProdTMA);
+        p->tma = sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA);
         if (!p->tma) {
             fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d", c.bn, c.cg);
             delete p;
@@ -271,7 +280,9 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     // Stream-K (TMA path, unsplit): every slot runs, whatever the tile count.
     if (e == cudaSuccess && c.sk && p->tma && p->splits == 1) {
         const sat::KernelEntry* t = p->tma;
-        const int64_t tiles = ((M + 128 * t->cg - 1) / (128 * t->cg)) * ((N + t->bn - 1) / t->bn);
+        int64_t tm = 0, tn = 0;
+        sat::tile_grid(t, M, N, &tm, &tn);
+        const int64_t tiles = tm * tn;
         const int64_t slots = slots_for(p, t);
         if (sat::sk_layout(tiles, num_kb, slots, &p->sk_tiles, &p->sk_w)) {
             p->sk_ctas = static_cast<int>(slots * t->cg);
@@ -302,10 +313,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     char sk_desc[48] = "";
     if (p->sk_tiles)
         std::snprintf(sk_desc, sizeof sk_desc, " sk%d/%d", p->sk_tiles, p->sk_w);
-    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s",
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s%s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
                   p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
-                  source, p->c_ring ? " cring" : "", sk_desc);
+                  source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "");
     return p;
 }
 
@@ -381,8 +392,10 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     a.C = C;
     a.alpha = alpha;
     a.beta = beta;
-    a.tiles_m = static_cast<int>((p->M + 128 * k->cg - 1) / (128 * k->cg));
-    a.tiles_n = static_cast<int>((p->N + k->bn - 1) / k->bn);
+    int64_t tiles_m = 0, tiles_n = 0;
+    sat::tile_grid(k, p->M, p->N, &tiles_m, &tiles_n);
+    a.tiles_m = static_cast<int>(tiles_m);
+    a.tiles_n = static_cast<int>(tiles_n);
     a.num_kb = static_cast<int>((p->K + k->bk - 1) / k->bk);
     a.splits = p->splits;
     a.kb_per_split = p->splits > 1 ? p->kb_per_split : a.num_kb;
@@ -444,7 +457,8 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         std::lock_guard<std::mutex> lock(p->mu);
         if (p->map_A != A) {
             const int rc =
-                encode_2d(&p->tmA, p->dt, A, p->K, p->M, static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B);
+                encode_2d(&p->tmA, p->dt, A, p->K, p->M, static_cast<uint32_t>(k->bk),
+                          k->prod == sat::kProdSwap ? static_cast<uint32_t>(k->bn) : 128u, CU_TENSOR_MAP_SWIZZLE_128B);
             if (rc) {
                 p->map_A = nullptr;
                 return rc;
@@ -558,8 +572,8 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
         return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
     const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
-    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
-                  c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.source == 1 ? "table" : "rule");
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.swap, c.source == 1 ? "table" : "rule");
     return GEMM_OK;
 }
 

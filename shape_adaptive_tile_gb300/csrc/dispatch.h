@@ -14,6 +14,7 @@ struct Choice {
     int splits;   // K splits (fixed-order reduction through a workspace); 0 or 1: none
     int cload;    // beta != 0: 1 = the epilogue loads C itself, 0 = the producer fetches it through the ring
     int sk;       // 1: stream-K for the last waves of tiles (fixed-order fix-up of split tiles)
+    int swap;     // 1: operand roles exchanged (the MMA computes C^T = B^T A^T; bn tiles M), 1-SM only
 };
 
 // Stream-K layout for T output tiles of KB k-blocks on G CTA slots: the

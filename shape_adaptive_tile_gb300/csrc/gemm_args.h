@@ -13,6 +13,7 @@ constexpr int kDtFP16 = 2;
 // Producer kinds.
 constexpr int kProdTMA = 0;    // TMA tensor loads (16-byte aligned bases and strides)
 constexpr int kProdPlain = 1;  // plain loads into the same swizzled layout (any stride)
+constexpr int kProdSwap = 2;   // TMA loads, operand roles exchanged: the MMA computes C^T = B^T A^T
 
 struct GemmArgs {
     int M, N, K;

@@ -42,6 +42,14 @@ constexpr uint32_t kErrTimeoutPartial = 1u << 4;   // a stream-K partial tile ne
 
 template <int DT, int BN, int CG, int PROD>
 struct Traits {
+    static constexpr bool TMA = PROD != kProdPlain;  // one elected thread issues TMA loads
+    // Operand roles exchanged: the tensor core computes C^T = B^T A^T, its
+    // 128 accumulator rows being 128 columns n of C and its BN columns BN
+    // rows m of C. The first MMA operand is B^T, read from B as it lies
+    // (n contiguous, MN-major); the second is A^T, read from A as it lies (k
+    // contiguous, K-major). For skinny M, where 128-row tiles of C would be
+    // mostly empty.
+    static constexpr bool SWAP = PROD == kProdSwap;
     static constexpr bool kTF32 = DT == kDtTF32;
     static constexpr int ES = kTF32 ? 4 : 2;        // bytes per operand element
     static constexpr int BM = 128;                  // accumulator rows per CTA
@@ -52,20 +60,21 @@ struct Traits {
     static constexpr int BN_CTA = BN / CG;          // B columns this CTA loads
     static constexpr int NBOX = BN_CTA / CW;        // B boxes per stage
     static constexpr int A_BYTES = BM * 128;
-    static constexpr int B_BYTES = NBOX * BK * 128;
+    static constexpr int NBOX_A = BM / CW;          // swapped: boxes of CW columns n of B per stage
+    static constexpr int B_BYTES = SWAP ? BN * 128 : NBOX * BK * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // Epilogue: 8 warps (4 with the plain-load producer), two (one) per TMEM
     // lane quarter, taking alternate 32-column chunks. Each has one 4 KB staging buffer: 32 rows x 128
     // bytes in the TMA store's 128-byte swizzle for the bulk-store path, or
     // a 32 x 32 XOR-swizzled transpose buffer for the row-store fallback.
-    static constexpr int EPI_WARPS = PROD == kProdTMA ? 8 : 4;   // plain-load CTAs keep 9 warps
+    static constexpr int EPI_WARPS = TMA ? 8 : 4;   // plain-load CTAs keep 9 warps
     static constexpr int EPI_WARP_BYTES = 4096;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
     static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    static constexpr int NPW = PROD == kProdTMA ? 1 : 4;   // producer warps
+    static constexpr int NPW = TMA ? 1 : 4;   // producer warps
     static constexpr int MMA_WARP = NPW;
     static constexpr int EPI_WARP0 = NPW + 1;
     static constexpr int THREADS = (NPW + 1 + EPI_WARPS) * 32;
@@ -87,7 +96,7 @@ struct Traits {
     // producer of tf32 instead stores B transposed, K-major like A.
     static constexpr bool B_MN = true;
     static constexpr uint32_t B_LAYOUT = kTF32 ? kLayoutSW128Atom32 : kLayoutSW128;
-    static constexpr uint32_t IDESC = idesc_f32acc(FMT, BM * CG, BN, B_MN);
+    static constexpr uint32_t IDESC = SWAP ? idesc_f32acc(FMT, BM, BN, false, true) : idesc_f32acc(FMT, BM * CG, BN, B_MN);
     // MN-major: 128-byte column blocks are BK*128 bytes apart (leading byte
     // offset); K rows come in swizzle groups, 8 rows (1024 bytes) for the
     // 16-byte-atom swizzle and 4 rows (512 bytes) for the 32-byte-atom one
@@ -99,10 +108,11 @@ struct Traits {
     static constexpr uint32_t B_KSTEP = B_MN ? UK * 128 : UK * ES;
     static constexpr uint32_t A_KSTEP = UK * ES;    // bytes per MMA step of K in A (= 32)
 
-    static_assert(BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
+    static_assert(SWAP || BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
+    static_assert(!SWAP || (CG == 1 && BN >= 32), "swapped tiles: 1-SM, whole 32-column chunks");
     static_assert(BN >= 16 && BN <= 256 && BN % 16 == 0, "MMA N");
     static_assert(STAGES >= 2, "ring too small");
-    static_assert(PROD == kProdTMA || CG == 1, "plain-load producer is 1-SM only");
+    static_assert(PROD != kProdPlain || CG == 1, "plain-load producer is 1-SM only");
     static_assert(2 * BN <= 512, "two accumulators must fit in TMEM");
 };
 
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
     static_assert(T::STAGES + 3 <= 32, "one lane per stage");
     if (warp == 0) {
         if (lane < T::STAGES) {
-            mbar_init(full_bar(lane), PROD == kProdTMA ? 1 : T::NPW * 32);
+            mbar_init(full_bar(lane), T::TMA ? 1 : T::NPW * 32);
             mbar_init(empty_bar(lane), 1);
             mbar_init(cfull_bar(lane), 1);
             c_readers[lane] = 0;
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         }
         fence_mbar_init();
     }
-    if (PROD == kProdTMA && warp == 0 && lane == 0) {
+    if (T::TMA && warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
 
     if (warp < T::NPW) {
         // ------------------------------------------------------------ producer
-        if constexpr (PROD == kProdTMA) {
+        if constexpr (T::TMA) {
             if (lane == 0) {
                 int stage = 0;
                 uint32_t phase = 0;
@@ -336,7 +346,16 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         }
                         const uint32_t fb = full0 + 8u * stage;
                         const int k0 = kb * T::BK;
-                        if constexpr (CG == 1) {
+                        if constexpr (T::SWAP) {
+                            // First operand: columns m0 .. m0 + 127 of B (the
+                            // tile's rows are columns of C), NBOX_A boxes of CW
+                            // columns; second: rows n0 .. n0 + BN - 1 of A.
+                            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
+#pragma unroll
+                            for (int j = 0; j < T::NBOX_A; ++j)
+                                tma_load_2d(sA + stage * T::A_BYTES + j * (T::BK * 128), &tmB, fb, m0 + j * T::CW, k0);
+                            tma_load_2d(sB + stage * T::B_BYTES, &tmA, fb, k0, n0);
+                        } else if constexpr (CG == 1) {
                             mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
                             tma_load_2d(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
 #pragma unroll
@@ -605,8 +624,12 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     const uint32_t b0 = sB + stage * T::B_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < T::KSTEPS; ++ks) {
-                        const uint64_t ad = sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
-                        const uint64_t bd = sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
+                        // Swapped: the first operand is MN-major (laid out as
+                        // B is otherwise), the second K-major (as A is).
+                        const uint64_t ad = T::SWAP ? sdesc(a0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT)
+                                                    : sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
+                        const uint64_t bd = T::SWAP ? sdesc(b0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128)
+                                                    : sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
                         mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb != w.kb0 || ks != 0) ? 1u : 0u);
                     }
                     issued = true;
@@ -691,8 +714,8 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
             // ahead (the first one before the accumulator wait); the
             // stream-K copy reads it only when the chunk is stored, after any
             // partial sums have been added, to keep its registers in bounds.
-            const bool prefetch_c = MODE == 0 && args.c_tma && beta != 0.0f;
-            const bool late_c = SK && args.c_tma && beta != 0.0f;
+            const bool prefetch_c = MODE == 0 && !T::SWAP && args.c_tma && beta != 0.0f;
+            const bool late_c = SK && !T::SWAP && args.c_tma && beta != 0.0f;
             // C through the ring: where the next unit's stages start, and per
             // stage the parity of its next C fill.
             int rpos = 0;
@@ -738,6 +761,20 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                 const int yoff = w.s * args.out_rows;
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
                                        static_cast<uint32_t>(acc * T::ACC_COLS);
+                if constexpr (NCHUNK < CSTEP) {
+                    // A tile narrower than the epilogue's warps: a warp with
+                    // no chunk still hands the accumulator back.
+                    if (half >= NCHUNK) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (CG == 1)
+                                mbar_arrive(tempty0 + 8u * acc);
+                            else
+                                mbar_arrive_cluster(tempty0 + 8u * acc);
+                        }
+                    }
+                }
 #pragma unroll 1
                 for (int c = half; c < NCHUNK; c += CSTEP) {
                     uint32_t r[32];
@@ -786,6 +823,55 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                                 }
                             }
                         }
+                    }
+                    if constexpr (T::SWAP) {
+                        // Swapped tile: this lane's accumulator row is column
+                        // ccol of C, and its 32 values are rows crow .. crow + 31.
+                        // For each row j the warp touches 32 consecutive floats.
+                        const int ccol = row0 + lane;
+                        const int crow = gcol0;
+                        float ct[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            ct[j] = beta != 0.0f && crow + j < args.M && ccol < args.N
+                                        ? args.C[static_cast<int64_t>(crow + j) * ldc + ccol]
+                                        : 0.0f;
+                        if (args.c_tma) {
+                            // Stage the 32 x 32 block of C (rows crow.., columns
+                            // row0..) in the store's 128-byte swizzle: row j, piece
+                            // lane / 4 at (lane / 4) ^ (j & 7); conflict free.
+                            if (lane == 0)
+                                bulk_wait_read<0>();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                float v = alpha * __uint_as_float(r[j]);
+                                if (beta != 0.0f)
+                                    v = fmaf(beta, ct[j], v);
+                                st_shared_f32(sb + static_cast<uint32_t>(j * 128 + ((((lane >> 2) ^ (j & 7)) << 4) |
+                                                                                    ((lane & 3) << 2))),
+                                              v);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && crow < args.M && row0 < args.N) {
+                                tma_store_2d(&tmC, sb, row0, yoff + crow);
+                                bulk_commit();
+                            }
+                        } else if (ccol < args.N) {
+                            float* cp = args.C + (static_cast<int64_t>(yoff) + crow) * ldc + ccol;
+                            const int rows = min(32, args.M - crow);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                if (j < rows) {
+                                    float v = alpha * __uint_as_float(r[j]);
+                                    if (beta != 0.0f)
+                                        v = fmaf(beta, ct[j], v);
+                                    cp[j * ldc] = v;
+                                }
+                            }
+                        }
+                        continue;
                     }
                     if (args.c_tma) {
                         // Bulk-store path: this thread owns row (row0 + lane) of the
@@ -896,10 +982,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         using Plain = std::integral_constant<int, 0>;
         using Ring = std::integral_constant<int, 1>;
         using StreamK = std::integral_constant<int, 2>;
-        if (PROD == kProdTMA && args.sk_tiles > 0) {
+        if (T::TMA && args.sk_tiles > 0) {
             // Stream-K pieces first, then the whole tiles in the plain copy
             // (the pieces' extra work does not weigh on its registers).
-            if constexpr (PROD == kProdTMA)
+            if constexpr (T::TMA)
                 tile_loop(StreamK{});
             tile_loop(Plain{});
         } else if (T::C_RING_OK && c_ring) {

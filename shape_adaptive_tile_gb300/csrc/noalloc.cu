@@ -138,8 +138,9 @@ int64_t slots_for(int sm_count, const sat::KernelEntry* e)
 
 int grid_for(int64_t M, int64_t N, int splits, int sm_count, const sat::KernelEntry* e)
 {
-    const int64_t tm = 128 * e->cg;
-    const int64_t units = ((M + tm - 1) / tm) * ((N + e->bn - 1) / e->bn) * splits;
+    int64_t tm = 0, tn = 0;
+    sat::tile_grid(e, M, N, &tm, &tn);
+    const int64_t units = tm * tn * splits;
     const int64_t slots = slots_for(sm_count, e);
     return static_cast<int>((units < slots ? units : slots) * e->cg);
 }
@@ -184,7 +185,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     const bool tma_ok = (K * es) % 16 == 0 && (N * es) % 16 == 0;
     const sat::Choice c = sat::select_config(M, N, K, dt, ds->sm_count, tma_ok);
     const bool use_tma = tma_ok && reinterpret_cast<uintptr_t>(A) % 16 == 0 && reinterpret_cast<uintptr_t>(B) % 16 == 0;
-    const sat::KernelEntry* k = use_tma ? sat::find_entry(dt, c.bn, c.cg, sat::kProdTMA)
+    const sat::KernelEntry* k = use_tma ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA)
                                         : sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
     if (!k)
         return fail(GEMM_ERR_ARG, "no compiled kernel for the chosen configuration");
@@ -207,7 +208,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     int sk_tiles = 0, sk_w = 0;
     int64_t sk_ctas = 0;
     if (c.sk && use_tma && splits == 1) {
-        const int64_t tiles = ((M + tile_rows - 1) / tile_rows) * ((N + k->bn - 1) / k->bn);
+        int64_t tm = 0, tn = 0;
+        sat::tile_grid(k, M, N, &tm, &tn);
+        const int64_t tiles = tm * tn;
         const int64_t slots = slots_for(ds->sm_count, k);
         if (sat::sk_layout(tiles, num_kb, slots, &sk_tiles, &sk_w)) {
             sk_ctas = slots * k->cg;
@@ -240,8 +243,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     a.C = splits > 1 ? ws : C;
     a.alpha = splits > 1 ? 1.0f : alpha;
     a.beta = splits > 1 ? 0.0f : beta;
-    a.tiles_m = static_cast<int>((M + 128 * k->cg - 1) / (128 * k->cg));
-    a.tiles_n = static_cast<int>((N + k->bn - 1) / k->bn);
+    int64_t tiles_m = 0, tiles_n = 0;
+    sat::tile_grid(k, M, N, &tiles_m, &tiles_n);
+    a.tiles_m = static_cast<int>(tiles_m);
+    a.tiles_n = static_cast<int>(tiles_n);
     a.num_kb = static_cast<int>(num_kb);
     a.splits = splits;
     a.kb_per_split = splits > 1 ? kbps : a.num_kb;
@@ -271,7 +276,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
         a.sk_epoch = 1;
     }
     if (use_tma) {
-        if (!encode(&tmA, tdt, es, A, K, M, static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        if (!encode(&tmA, tdt, es, A, K, M, static_cast<uint32_t>(k->bk),
+                    k->prod == sat::kProdSwap ? static_cast<uint32_t>(k->bn) : 128u, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tmB, tdt, es, B, N, K, static_cast<uint32_t>(128 / es), static_cast<uint32_t>(k->bk),
                     static_cast<CUtensorMapSwizzle>(k->b_swizzle)))
             return fail(GEMM_ERR_LAUNCH, "encoding the operand tensor maps");

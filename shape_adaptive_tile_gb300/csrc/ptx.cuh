@@ -273,6 +273,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float a)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float& a, float& b, float& c, float& d)
 {
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr) : "memory");
@@ -337,10 +342,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 // accumulator: D format (bits 4-5) = F32, A/B formats (bits 7-9, 10-12),
 // A K-major (bit 15 = 0), B major-ness (bit 16: 1 = MN-major), N >> 3
 // (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_format, int M, int N, bool b_mn_major)
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_format, int M, int N, bool b_mn_major,
+                                                    bool a_mn_major = false)
 {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (0u << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // A/B format codes of the instruction descriptor.

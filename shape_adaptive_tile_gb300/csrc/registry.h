@@ -13,7 +13,7 @@ struct KernelEntry {
     int dt;        // kDtTF32 / kDtBF16 / kDtFP16
     int bn;        // N of the output tile
     int cg;        // 1: one SM per 128-row tile; 2: a CTA pair (cluster of 2) per 256-row tile
-    int prod;      // kProdTMA / kProdPlain
+    int prod;      // kProdTMA / kProdPlain / kProdSwap
     int stages;    // shared-memory ring depth
     int threads;   // CTA size
     int smem;      // dynamic shared memory bytes
@@ -39,6 +39,16 @@ void set_last_error(const char* msg);
 
 // Finds the variant, or nullptr.
 const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
+
+// The output tiles of a variant, as rows of tiles (the accumulator's 128 x
+// cta_group rows) and columns of tiles (its bn columns). A swapped variant
+// tiles C^T: 128 columns of C by bn rows.
+inline void tile_grid(const KernelEntry* e, int64_t M, int64_t N, int64_t* tiles_m, int64_t* tiles_n)
+{
+    const int64_t rows = e->prod == kProdSwap ? N : M, cols = e->prod == kProdSwap ? M : N;
+    *tiles_m = (rows + 128 * e->cg - 1) / (128 * e->cg);
+    *tiles_n = (cols + e->bn - 1) / e->bn;
+}
 
 // Defined in aux_kernels.cu.
 cudaError_t launch_scale(float* C, long long n, float beta, cudaStream_t stream);

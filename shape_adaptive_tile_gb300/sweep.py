@@ -37,6 +37,8 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
     for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
         if not tma_ok and (cg == 2 or bn == 64):
             continue
+        if cg == 2 and M <= 128:
+            continue
         tiles = -(-M // (128 * cg)) * -(-N // bn)
         slots = sm_count // cg
         for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
@@ -55,6 +57,17 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
             if ctas * s <= 2 * sm_count and kb // s >= 4:
                 for group in (2, 8):
                     out.append(f"{bn},{cg},0,{group},{s}")
+    # Skinny M: operand roles exchanged, tiles of 128 columns by bn rows of C.
+    if tma_ok and M <= 128:
+        for bn in (32, 64, 128):
+            if bn > 2 * M and bn > 32:
+                continue
+            tiles = -(-N // 128) * -(-M // bn)
+            for raster, group in itertools.product((0, 1), (2, 8)):
+                out.append(f"{bn},1,{raster},{group},swap")
+            for s in (2, 4, 8):
+                if tiles * s <= 2 * sm_count and kb // s >= 4:
+                    out.append(f"{bn},1,0,8,{s},swap")
     return out
 
 
@@ -105,8 +118,9 @@ def table_row(e):
     splits = nums[0] if nums else "1"
     cload = 1 if "cload" in parts[4:] else 0
     sk = 1 if "sk" in parts[4:] else 0
+    swap = 1 if "swap" in parts[4:] else 0
     return (f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}, "
-            f"{cload}, {sk}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+            f"{cload}, {sk}, {swap}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
 
 
 def _key(line):
@@ -126,7 +140,7 @@ def write_table(entries, path=TABLE, merge=False):
                     rows[k] = line.rstrip("\n")
     for e in entries:
         rows[(DT_CODE[e["dtype"]], e["M"], e["N"], e["K"])] = table_row(e)
-    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload, sk}}.",
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload, sk, swap}}.",
              "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
              "// (median of L2-flushed runs) of every candidate configuration."]
     order = {1: 0, 2: 1, 0: 2}  # bf16, fp16, tf32

@@ -164,6 +164,10 @@ WORKLOADS = [
     ("square8192", "bf16", (8192, 8192, 8192), "normal", 1.0, 0.0, None, 3, "rel_rms"),
     ("square4096", "fp16", (4096, 4096, 4096), "normal", 1.0, 0.0, None, 3, "rel_rms"),
     ("square8192", "fp16", (8192, 8192, 8192), "normal", 1.0, 0.0, None, 3, "rel_rms"),
+    # skinny M (few rows against wide, deep operands), where the dispatcher
+    # may exchange the operands' roles
+    ("skinny16x8192x8192", "bf16", (16, 8192, 8192), "normal", 1.0, 0.0, None, 5, "rel_rms"),
+    ("skinny32x16384x4096", "tf32", (32, 16384, 4096), "normal", 1.0, 0.0, None, 5, "rel_rms"),
 ] + [
     (f"tail{M}x{N}x{K}", dt, (M, N, K), "uniform", 1.5, 0.5, "normal", 4, "rel_rms")
     for dt in ("tf32", "bf16")

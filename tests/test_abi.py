@@ -54,20 +54,37 @@ def test_plan_create_fails_cleanly_without_a_gpu(lib):
 
 
 def _choice(M, N, K, dt, sms=152, tma=True):
-    bn, cg, raster, group, splits, cload, sk, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
+    bn, cg, raster, group, splits, cload, sk, swap, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
     return int(bn), int(cg), int(raster), int(group), int(splits), source
+
+
+def _swap(M, N, K, dt, tma=True):
+    return int(sat.gemm_select_config(M, N, K, dt, 152, tma).split(",")[7])
 
 
 @pytest.mark.parametrize("dt", ["tf32", "bf16", "fp16"])
 def test_dispatcher_choices_are_compiled_variants(dt):
     for M, N, K in [(256, 256, 256), (2048, 2048, 2048), (8192, 8192, 8192), (768, 768, 768),
-                    (8191, 4097, 2049), (16384, 1024, 4096), (128, 8192, 8192), (4096, 4096, 512), (1, 1, 1)]:
+                    (8191, 4097, 2049), (16384, 1024, 4096), (128, 8192, 8192), (4096, 4096, 512), (1, 1, 1),
+                    (16, 8192, 8192), (64, 4096, 520)]:
         for tma in (True, False):
             bn, cg, raster, group, splits, _ = _choice(M, N, K, dt, tma=tma)
-            assert bn in (64, 128, 256) and cg in (1, 2) and raster in (0, 1) and group >= 1
+            swap = _swap(M, N, K, dt, tma)
+            assert cg in (1, 2) and raster in (0, 1) and group >= 1
             assert 1 <= splits <= 16
+            if swap:   # swapped variants: 1-SM, 32/64/128 rows of C per tile
+                assert tma and cg == 1 and bn in (32, 64, 128)
+            else:
+                assert bn in (64, 128, 256)
             if not tma:
                 assert cg == 1 and bn in (128, 256)   # plain-load producer exists only for these
+
+
+def test_dispatcher_swaps_operands_for_skinny_m_only():
+    assert _swap(1, 4096, 4096, "tf32") == 1 and _choice(1, 4096, 4096, "tf32")[0] == 32
+    assert _swap(32, 4096, 4096, "bf16") == 1 and _choice(32, 4096, 4096, "bf16")[0] == 32
+    assert _swap(48, 4096, 4096, "bf16") == 0
+    assert _swap(16, 4100, 4096, "bf16", tma=False) == 0   # no TMA, no swapped variant
 
 
 def test_dispatcher_fills_the_machine_for_skinny_m():

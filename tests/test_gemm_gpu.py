@@ -29,7 +29,8 @@ CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,
            "128,1,0,8,cload", "64,1,1,4,cload", "256,2,0,4,cload", "128,2,1,2,cload",
            "256,1,0,8,plain", "128,1,1,3,plain",
            "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain",
-           "256,2,0,4,sk", "128,1,0,8,sk", "64,1,1,4,sk"]
+           "256,2,0,4,sk", "128,1,0,8,sk", "64,1,1,4,sk",
+           "128,1,0,4,swap", "64,1,1,2,swap", "32,1,0,8,swap", "64,1,0,2,3,swap"]
 SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
 
 
@@ -151,6 +152,38 @@ def test_stream_k_with_c_not_16_byte_aligned():
         torch.cuda.synchronize()
         sat.check(plan.status())
     checks.assert_bit_exact(flatC[1:].view(M, N).cpu().numpy(), ref32, "stream-K, C misaligned")
+
+
+# Skinny M through the dispatcher's own choice: operand roles exchanged, the
+# tensor core computing C^T in tiles of 128 columns by 32 or 64 rows, with
+# ragged N and K tails (and a K split where the tiles leave SMs idle).
+@pytest.mark.parametrize("dtype,M,N,K,config", [("bf16", 1, 4104, 520, None), ("tf32", 16, 4100, 516, None),
+                                                ("fp16", 33, 2056, 1032, "64,1,0,8,swap"),
+                                                ("bf16", 64, 1000, 4104, "64,1,1,4,4,swap"),
+                                                ("tf32", 7, 260, 8196, None)])
+def test_skinny_m_swapped_operands(dtype, M, N, K, config):
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 61, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+    assert " swap" in desc
+    checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+    A, B, C0 = si.problem(M, N, K, dtype, "normal", 62, "normal")
+    ref64, _ = oracle.gemm(A, B, C0, 1.0, -1.0, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.0, -1.0, config)
+    checks.assert_rel_rms(got, ref64, si.REL_RMS_BOUND[dtype], f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+def test_swapped_operands_with_c_not_16_byte_aligned():
+    M, N, K = 24, 520, 264
+    A, B, C0 = si.problem(M, N, K, "bf16", "dyadic", 63, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, "bf16")
+    flatC = to_dev(np.concatenate([np.zeros(1, np.float32), C0.ravel()]))
+    with sat.Plan(M, N, K, "bf16") as plan:
+        assert " swap" in plan.describe()
+        run(plan, to_dev(A, "bf16"), to_dev(B, "bf16"), flatC.data_ptr() + 4, 1.5, -0.5)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    checks.assert_bit_exact(flatC[1:].view(M, N).cpu().numpy(), ref32, "swapped, C misaligned")
 
 
 def test_k_zero_and_alpha_zero_scale_c():

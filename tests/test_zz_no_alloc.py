@@ -30,6 +30,7 @@ CASES = [
     ("fp16", 513, 264, 130, "dyadic", 1.0, 1.0),
     ("bf16", 333, 517, 389, "uniform", 1.5, 0.5),    # misaligned row strides: plain-load producer
     ("bf16", 6144, 6144, 4096, "normal", 1.0, 0.0),  # stream-K: partial tiles and counters in the scratch
+    ("bf16", 16, 8192, 8192, "dyadic", 1.5, 0.5),    # skinny M: operands swapped, K split in the scratch
 ]
 
 
@@ -70,7 +71,7 @@ def test_noalloc_matches_gemm_run_on_two_calls(case):
 
 def _split_workspace_bytes(M, N, K, dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    bn, cg, _, _, splits, _, _, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
+    bn, cg, _, _, splits, _, _, swap, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
     rows = 128 * int(cg)
     return int(splits), int(splits) * (-(-M // rows) * rows) * N * 4
 
