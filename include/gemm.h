@@ -85,6 +85,20 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
 gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config);
 
 /*
+ * As gemm_plan_create_config, for C = alpha * op(A) * op(B) + beta * C where
+ * op(A) is M x K and op(B) is K x N: trans_a != 0 means A is stored as its
+ * transpose (K x M, row-major), trans_b != 0 that B is (N x K, row-major).
+ * Transposed operands are read by TMA only (no plain-load kernel exists for
+ * them), so every gemm_run_ex of such a plan needs A and B 16-byte aligned
+ * with row strides that are multiples of 16 bytes (GEMM_ERR_ALIGN
+ * otherwise). Tiles with transposed operands are 1-SM 128 x 128 or
+ * 128 x 256, or CTA-pair 256 x 256; a configuration naming another tile N
+ * is rounded to one of these, and ",swap" is ignored. `config` may be NULL.
+ */
+gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int trans_a, int trans_b,
+                               const char* config);
+
+/*
  * Enqueue C = alpha * A * B + beta * C on `cuda_stream` (a cudaStream_t; NULL
  * is the legacy default stream) and return without synchronising.
  *   A: device pointer, M x K elements of the plan's dtype, row-major.
@@ -108,6 +122,18 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
  */
 int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, float alpha, float beta,
              void* cuda_stream);
+
+/*
+ * gemm_run with row strides (leading dimensions, in elements): lda for A as
+ * stored (>= K, or >= M when the plan has A transposed), ldb for B as stored
+ * (>= N, or >= K when transposed), ldc for C (>= N, in floats). gemm_run is
+ * this call with the dense strides. Operands whose row strides are not
+ * 16-byte multiples take the plain-load path (untransposed plans only); C
+ * whose row stride is not a 16-byte multiple takes the row-store epilogue.
+ * GEMM_ERR_ARG for a stride below the minimum.
+ */
+int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+                float alpha, float beta, void* cuda_stream);
 
 /*
  * End-to-end form of gemm_run for operands in HOST memory (pinned host

@@ -23,8 +23,8 @@ STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_ARG", -2: "GEMM_ERR_ARCH", -3: "GEMM_ERR_A
           -4: "GEMM_ERR_LAUNCH", -5: "GEMM_ERR_TIMEOUT", -6: "GEMM_ERR_NOMEM"}
 
 # Every function the C ABI exports (include/gemm.h).
-EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_run", "gemm_run_host",
-           "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
+EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_plan_create_ex", "gemm_run", "gemm_run_ex",
+           "gemm_run_host", "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
            "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc")
 
 _lock = threading.Lock()
@@ -52,6 +52,10 @@ def lib() -> ctypes.CDLL:
             L.gemm_plan_create_config.restype = vp
             L.gemm_run.argtypes = [vp, vp, vp, vp, f32, f32, vp]
             L.gemm_run.restype = i32
+            L.gemm_plan_create_ex.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.c_char_p]
+            L.gemm_plan_create_ex.restype = vp
+            L.gemm_run_ex.argtypes = [vp, vp, i64, vp, i64, vp, i64, f32, f32, vp]
+            L.gemm_run_ex.restype = i32
             L.gemm_run_host.argtypes = [vp, vp, vp, vp, f32, f32, vp, vp, vp, vp]
             L.gemm_run_host.restype = i32
             L.gemm_plan_destroy.argtypes = [vp]
@@ -100,8 +104,21 @@ def gemm_plan_create_config(M: int, N: int, K: int, dtype, config: str | None) -
     return h
 
 
+def gemm_plan_create_ex(M: int, N: int, K: int, dtype, trans_a: bool, trans_b: bool, config: str | None = None) -> int:
+    h = lib().gemm_plan_create_ex(M, N, K, _dt(dtype), int(bool(trans_a)), int(bool(trans_b)),
+                                  config.encode() if config else None)
+    if not h:
+        raise GemmError(-1, gemm_last_error())
+    return h
+
+
 def gemm_run(plan: int, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> int:
     return lib().gemm_run(plan, _p(A), _p(B), _p(C), alpha, beta, _p(stream))
+
+
+def gemm_run_ex(plan: int, A, lda: int, B, ldb: int, C, ldc: int, alpha: float = 1.0, beta: float = 0.0,
+                stream=None) -> int:
+    return lib().gemm_run_ex(plan, _p(A), lda, _p(B), ldb, _p(C), ldc, alpha, beta, _p(stream))
 
 
 def gemm_run_host(plan: int, hA, hB, hC, alpha, beta, dA, dB, dC, stream=None) -> int:
@@ -145,12 +162,26 @@ def check(status: int) -> None:
 class Plan:
     """Owns one gemm_plan; ``run`` takes device tensors (or raw pointers)."""
 
-    def __init__(self, M: int, N: int, K: int, dtype, config: str | None = None):
+    def __init__(self, M: int, N: int, K: int, dtype, config: str | None = None, trans_a: bool = False,
+                 trans_b: bool = False):
         self.M, self.N, self.K, self.dtype = M, N, K, dtype
-        self.handle = gemm_plan_create_config(M, N, K, dtype, config)
+        self.trans_a, self.trans_b = trans_a, trans_b
+        if trans_a or trans_b:
+            self.handle = gemm_plan_create_ex(M, N, K, dtype, trans_a, trans_b, config)
+        else:
+            self.handle = gemm_plan_create_config(M, N, K, dtype, config)
 
-    def run(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
-        check(gemm_run(self.handle, A, B, C, alpha, beta, stream))
+    def run(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, lda: int | None = None,
+            ldb: int | None = None, ldc: int | None = None) -> None:
+        """C = alpha * op(A) * op(B) + beta * C; the leading dimensions
+        default to the dense ones."""
+        if lda is None and ldb is None and ldc is None:
+            check(gemm_run(self.handle, A, B, C, alpha, beta, stream))
+            return
+        lda = lda if lda is not None else (self.M if self.trans_a else self.K)
+        ldb = ldb if ldb is not None else (self.K if self.trans_b else self.N)
+        ldc = ldc if ldc is not None else self.N
+        check(gemm_run_ex(self.handle, A, lda, B, ldb, C, ldc, alpha, beta, stream))
 
     def status(self) -> int:
         return gemm_plan_status(self.handle)

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <new>
@@ -56,7 +57,7 @@ const char* dt_name(int dt) { return dt == 0 ? "tf32" : dt == 1 ? "bf16" : "fp16
 // 2-D row-major tensor map with a 128-byte-swizzled box of box_inner x
 // box_outer elements; out-of-bounds elements of a box read as zero.
 int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, CUtensorMapSwizzle swizzle)
+              uint32_t box_outer, CUtensorMapSwizzle swizzle, uint64_t ld = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -65,7 +66,7 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t inner, uint64_
                                   : dt == sat::kDtBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_size(dt))};
+    const cuuint64_t strides[1] = {(ld ? ld : inner) * static_cast<uint64_t>(elem_size(dt))};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -95,6 +96,7 @@ struct gemm_plan {
     int dt = 0;
     int device = 0;
     int sm_count = 0;
+    bool trans_a = false, trans_b = false;  // A stored K x M, B stored N x K
     sat::Choice choice{};
     bool force_plain = false;
     bool c_ring = false;  // beta != 0: the producer fetches C through the operand ring
@@ -120,6 +122,7 @@ struct gemm_plan {
     mutable const void* map_A = nullptr;
     mutable const void* map_B = nullptr;
     mutable const void* map_C = nullptr;
+    mutable int64_t map_lda = 0, map_ldb = 0, map_ldc = 0;
     mutable CUtensorMap tmA{}, tmB{}, tmC{};
 };
 
@@ -148,7 +151,8 @@ int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
     return static_cast<int>((tiles < slots ? tiles : slots) * e->cg);
 }
 
-gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config)
+gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config, bool trans_a = false,
+                  bool trans_b = false)
 {
     g_err[0] = '\0';
     const int dt = static_cast<int>(dtype);
@@ -189,8 +193,13 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     p->dt = dt;
     p->device = dev;
     p->sm_count = sms;
+    p->trans_a = trans_a;
+    p->trans_b = trans_b;
     const int64_t es = elem_size(dt);
-    const bool tma_ok = (K * es) % 16 == 0 && (N * es) % 16 == 0;
+    // Dense row strides that TMA can describe. Transposed operands are read
+    // by TMA only, so their plans assume it (gemm_run_ex checks each call).
+    const bool trans = trans_a || trans_b;
+    const bool tma_ok = trans || ((K * es) % 16 == 0 && (N * es) % 16 == 0);
 
     const char* source = "rule";
     if (config && config[0]) {
@@ -226,20 +235,39 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
         source = p->choice.source == 1 ? "table" : "rule";
     }
-    const sat::Choice& c = p->choice;
-    if (tma_ok && !p->force_plain) {
-        p->tma = sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA);
-        if (!p->tma) {
-            fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d", c.bn, c.cg);
+    if (trans) {
+        // Transposed layouts come as 1-SM 128 x 128 and 128 x 256 tiles and
+        // 256 x 256 CTA-pair tiles, unswapped, with TMA loads only.
+        sat::Choice& cc = p->choice;
+        cc.swap = 0;
+        cc.bn = cc.cg == 2 ? 256 : (cc.bn < 256 ? 128 : 256);
+        if (p->force_plain) {
+            fail(GEMM_ERR_ARG, "transposed operands have no plain-load kernel");
             delete p;
             return nullptr;
         }
     }
-    p->plain = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
-    if (!p->plain) {
-        fail(GEMM_ERR_ARG, "no compiled plain-load kernel for bn=%d", c.bn);
-        delete p;
-        return nullptr;
+    const sat::Choice& c = p->choice;
+    const int tma_kind = trans_a && trans_b ? sat::kProdTT
+                         : trans_a          ? sat::kProdTN
+                         : trans_b          ? sat::kProdNT
+                         : c.swap           ? sat::kProdSwap
+                                            : sat::kProdTMA;
+    if (tma_ok && !p->force_plain) {
+        p->tma = sat::find_entry(dt, c.bn, c.cg, tma_kind);
+        if (!p->tma) {
+            fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d in this layout", c.bn, c.cg);
+            delete p;
+            return nullptr;
+        }
+    }
+    if (!trans) {
+        p->plain = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
+        if (!p->plain) {
+            fail(GEMM_ERR_ARG, "no compiled plain-load kernel for bn=%d", c.bn);
+            delete p;
+            return nullptr;
+        }
     }
     for (const sat::KernelEntry* k : {p->tma, p->plain}) {
         if (!k)
@@ -263,7 +291,8 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         p->splits = static_cast<int>((num_kb + p->kb_per_split - 1) / p->kb_per_split);
     if (p->tma)
         p->grid_tma = grid_for(p, p->tma);
-    p->grid_plain = grid_for(p, p->plain);
+    if (p->plain)
+        p->grid_plain = grid_for(p, p->plain);
     e = cudaMalloc(&p->d_err, sizeof(uint32_t));
     if (e == cudaSuccess)
         e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
@@ -313,52 +342,28 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     char sk_desc[48] = "";
     if (p->sk_tiles)
         std::snprintf(sk_desc, sizeof sk_desc, " sk%d/%d", p->sk_tiles, p->sk_w);
-    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s%s",
+    std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s%s%s%s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
                   p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
-                  source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "");
+                  source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "",
+                  trans_a ? " ta" : "", trans_b ? " tb" : "");
     return p;
 }
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
-{
-    return create(M, N, K, dtype, nullptr);
-}
-
-gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config)
-{
-    return create(M, N, K, dtype, config);
-}
-
-void gemm_plan_destroy(gemm_plan* plan)
-{
-    if (!plan)
-        return;
-    if (plan->d_err)
-        cudaFree(plan->d_err);
-    if (plan->ws)
-        cudaFree(plan->ws);
-    if (plan->sk_ws)
-        cudaFree(plan->sk_ws);
-    if (plan->sk_flags)
-        cudaFree(plan->sk_flags);
-    delete plan;
-}
-
-const char* gemm_plan_describe(const gemm_plan* plan) { return plan ? plan->desc : ""; }
-
-const char* gemm_last_error(void) { return g_err; }
-
-int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float alpha, float beta, void* cuda_stream)
+int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+             float alpha, float beta, void* cuda_stream)
 {
     if (!p)
         return fail(GEMM_ERR_ARG, "plan is NULL");
     if (p->M == 0 || p->N == 0)
         return GEMM_OK;
+    if ((p->K > 0 && (lda < (p->trans_a ? p->M : p->K) || ldb < (p->trans_b ? p->K : p->N))) || ldc < p->N)
+        return fail(GEMM_ERR_ARG, "leading dimension too small (lda %lld, ldb %lld, ldc %lld)", (long long)lda,
+                    (long long)ldb, (long long)ldc);
     if (!C)
         return fail(GEMM_ERR_ARG, "C is NULL");
     if (reinterpret_cast<uintptr_t>(C) % 4 != 0)
@@ -371,7 +376,7 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         return fail(GEMM_ERR_ARG, "plan was made for device %d but device %d is current", p->device, dev);
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (p->K == 0 || alpha == 0.0f) {
-        e = sat::launch_scale(C, static_cast<long long>(p->M * p->N), beta, stream);
+        e = sat::launch_scale(C, p->M, p->N, ldc, beta, stream);
         return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the beta-scale kernel");
     }
     if (!A || !B)
@@ -379,8 +384,14 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     const uintptr_t es = static_cast<uintptr_t>(elem_size(p->dt));
     if (reinterpret_cast<uintptr_t>(A) % es || reinterpret_cast<uintptr_t>(B) % es)
         return fail(GEMM_ERR_ALIGN, "A and B must be aligned to their %d-byte element size", (int)es);
-    const bool use_tma =
-        p->tma && reinterpret_cast<uintptr_t>(A) % 16 == 0 && reinterpret_cast<uintptr_t>(B) % 16 == 0;
+    // TMA needs 16-byte aligned bases and row strides.
+    const bool use_tma = p->tma && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(B) % 16 == 0 && (lda * static_cast<int64_t>(es)) % 16 == 0 &&
+                         (ldb * static_cast<int64_t>(es)) % 16 == 0;
+    if (!use_tma && !p->plain)
+        return fail(GEMM_ERR_ALIGN,
+                    "transposed operands are read by TMA only: A and B must be 16-byte aligned with row strides "
+                    "that are multiples of 16 bytes");
     const sat::KernelEntry* k = use_tma ? p->tma : p->plain;
 
     sat::GemmArgs a{};
@@ -390,6 +401,9 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     a.A = A;
     a.B = B;
     a.C = C;
+    a.lda = lda;
+    a.ldb = ldb;
+    a.ldc = ldc;
     a.alpha = alpha;
     a.beta = beta;
     int64_t tiles_m = 0, tiles_n = 0;
@@ -406,6 +420,7 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         // The GEMM writes raw fp32 partial tiles to the workspace; the
         // reduction applies alpha and beta.
         a.C = p->ws;
+        a.ldc = p->N;
         a.alpha = 1.0f;
         a.beta = 0.0f;
         a.out_rows = p->ws_rows;
@@ -417,7 +432,8 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
 
     // C goes through the bulk-store epilogue when its base and row stride
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
-    const bool c_tma = split ? p->ws_tma : (p->N * 4) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+    const bool c_tma =
+        split ? p->ws_tma : p->N % 4 == 0 && ldc % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
     if (use_tma && p->sk_tiles > 0) {
@@ -443,36 +459,47 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
         tmC = p->tmW;
     } else if (c_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
-        if (p->map_C != C) {
-            const int rc = encode_2d(&p->tmC, sat::kDtTF32, C, p->N, p->M, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (p->map_C != C || p->map_ldc != ldc) {
+            const int rc =
+                encode_2d(&p->tmC, sat::kDtTF32, C, p->N, p->M, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B, ldc);
             if (rc) {
                 p->map_C = nullptr;
                 return rc;
             }
             p->map_C = C;
+            p->map_ldc = ldc;
         }
         tmC = p->tmC;
     }
     if (use_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
-        if (p->map_A != A) {
-            const int rc =
-                encode_2d(&p->tmA, p->dt, A, p->K, p->M, static_cast<uint32_t>(k->bk),
-                          k->prod == sat::kProdSwap ? static_cast<uint32_t>(k->bn) : 128u, CU_TENSOR_MAP_SWIZZLE_128B);
+        // Each operand as it lies: K contiguous (boxes of BK x rows, 128-byte
+        // swizzle) or M/N contiguous (boxes of 128 bytes x BK, the MN-major
+        // swizzle of the dtype).
+        const uint32_t cw = static_cast<uint32_t>(128 / es), bk = static_cast<uint32_t>(k->bk);
+        const CUtensorMapSwizzle mn_swz = static_cast<CUtensorMapSwizzle>(k->b_swizzle);
+        if (p->map_A != A || p->map_lda != lda) {
+            const int rc = p->trans_a ? encode_2d(&p->tmA, p->dt, A, p->M, p->K, cw, bk, mn_swz, lda)
+                                      : encode_2d(&p->tmA, p->dt, A, p->K, p->M, bk,
+                                                  k->prod == sat::kProdSwap ? static_cast<uint32_t>(k->bn) : 128u,
+                                                  CU_TENSOR_MAP_SWIZZLE_128B, lda);
             if (rc) {
                 p->map_A = nullptr;
                 return rc;
             }
             p->map_A = A;
+            p->map_lda = lda;
         }
-        if (p->map_B != B) {
-            const int rc = encode_2d(&p->tmB, p->dt, B, p->N, p->K, static_cast<uint32_t>(128 / es),
-                                     static_cast<uint32_t>(k->bk), static_cast<CUtensorMapSwizzle>(k->b_swizzle));
+        if (p->map_B != B || p->map_ldb != ldb) {
+            const int rc = p->trans_b ? encode_2d(&p->tmB, p->dt, B, p->K, p->N, bk,
+                                                  static_cast<uint32_t>(k->bn / k->cg), CU_TENSOR_MAP_SWIZZLE_128B, ldb)
+                                      : encode_2d(&p->tmB, p->dt, B, p->N, p->K, cw, bk, mn_swz, ldb);
             if (rc) {
                 p->map_B = nullptr;
                 return rc;
             }
             p->map_B = B;
+            p->map_ldb = ldb;
         }
         tmA = p->tmA;
         tmB = p->tmB;
@@ -481,12 +508,65 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the GEMM kernel");
     if (split) {
-        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C,
-                                      static_cast<long long>(p->M * p->N), alpha, beta, p->sm_count, stream);
+        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->M, p->N,
+                                      ldc, alpha, beta, p->sm_count, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the split-K reduction");
     }
     return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
+{
+    return create(M, N, K, dtype, nullptr);
+}
+
+gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config)
+{
+    return create(M, N, K, dtype, config);
+}
+
+gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int trans_a, int trans_b,
+                               const char* config)
+{
+    return create(M, N, K, dtype, config, trans_a != 0, trans_b != 0);
+}
+
+void gemm_plan_destroy(gemm_plan* plan)
+{
+    if (!plan)
+        return;
+    if (plan->d_err)
+        cudaFree(plan->d_err);
+    if (plan->ws)
+        cudaFree(plan->ws);
+    if (plan->sk_ws)
+        cudaFree(plan->sk_ws);
+    if (plan->sk_flags)
+        cudaFree(plan->sk_flags);
+    delete plan;
+}
+
+const char* gemm_plan_describe(const gemm_plan* plan) { return plan ? plan->desc : ""; }
+
+const char* gemm_last_error(void) { return g_err; }
+
+
+int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float alpha, float beta, void* cuda_stream)
+{
+    if (!p)
+        return fail(GEMM_ERR_ARG, "plan is NULL");
+    return run_impl(p, A, p->trans_a ? p->M : p->K, B, p->trans_b ? p->K : p->N, C, p->N, alpha, beta, cuda_stream);
+}
+
+int gemm_run_ex(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+                float alpha, float beta, void* cuda_stream)
+{
+    return run_impl(p, A, lda, B, ldb, C, ldc, alpha, beta, cuda_stream);
 }
 
 int gemm_run_host(const gemm_plan* p, const void* hA, const void* hB, float* hC, float alpha, float beta, void* dA,

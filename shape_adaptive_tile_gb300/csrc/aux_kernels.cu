@@ -7,76 +7,86 @@
 
 namespace sat {
 
-__global__ void sat_scale_kernel(float* __restrict__ C, long long n, float beta)
+__global__ void sat_scale_kernel(float* __restrict__ C, long long rows, long long cols, long long ldc, float beta)
 {
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
-        C[i] = beta == 0.0f ? 0.0f : beta * C[i];
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        float* row = C + r * ldc;
+        for (long long c = threadIdx.x; c < cols; c += blockDim.x)
+            row[c] = beta == 0.0f ? 0.0f : beta * row[c];
+    }
 }
 
-cudaError_t launch_scale(float* C, long long n, float beta, cudaStream_t stream)
+cudaError_t launch_scale(float* C, long long rows, long long cols, long long ldc, float beta, cudaStream_t stream)
 {
-    if (n <= 0)
+    if (rows <= 0 || cols <= 0)
         return cudaSuccess;
-    long long blocks = (n + 255) / 256;
-    if (blocks > 4096)
-        blocks = 4096;
-    sat_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, n, beta);
+    const long long blocks = rows < 8192 ? rows : 8192;
+    sat_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, rows, cols, ldc, beta);
     return cudaGetLastError();
 }
 
-// Split-K reduction: C[i] = alpha * (W_0[i] + W_1[i] + ... + W_{S-1}[i]) + beta * C[i],
-// summed in the fixed order s = 0, 1, ..., S-1 so that the result is the same on
-// every run. W_s is slice s of the workspace (`slice` floats apart, same row
-// stride N as C). beta == 0 never reads C. Memory-bound: S + 1 (+1) floats
-// of traffic per output element.
-__global__ void sat_splitk_reduce_kernel(const float* __restrict__ ws, int S, long long slice, float* C, long long n,
-                                         float alpha, float beta)
+// Split-K reduction: C[r][c] = alpha * (W_0[r][c] + W_1[r][c] + ... + W_{S-1}[r][c])
+// + beta * C[r][c], summed in the fixed order s = 0, 1, ..., S-1 so that the
+// result is the same on every run. W_s is slice s of the workspace (`slice`
+// floats apart, rows of `cols` floats); C has row stride ldc. beta == 0 never
+// reads C. Memory-bound: S + 1 (+1) floats of traffic per output element.
+// Each thread takes four consecutive columns of one row, as one 16-byte
+// access where the columns, the strides and C allow it.
+__global__ void sat_splitk_reduce_kernel(const float* __restrict__ ws, int S, long long slice, float* C,
+                                         long long rows, long long cols, long long ldc, float alpha, float beta)
 {
+    const long long c4 = (cols + 3) / 4;
+    const bool vec = cols % 4 == 0 && ldc % 4 == 0 && slice % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const long long n4 = (reinterpret_cast<uintptr_t>(C) % 16 == 0 && slice % 4 == 0) ? n / 4 : 0;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        float4 a = reinterpret_cast<const float4*>(ws)[i];
-        for (int s = 1; s < S; ++s) {
-            const float4 b = reinterpret_cast<const float4*>(ws + s * slice)[i];
-            a.x += b.x;
-            a.y += b.y;
-            a.z += b.z;
-            a.w += b.w;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * c4; i += stride) {
+        const long long r = i / c4, c = (i - r * c4) * 4;
+        const float* w = ws + r * cols + c;
+        float* o = C + r * ldc + c;
+        if (vec) {
+            float4 a = *reinterpret_cast<const float4*>(w);
+            for (int s = 1; s < S; ++s) {
+                const float4 b = *reinterpret_cast<const float4*>(w + s * slice);
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            }
+            float4 v = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
+            if (beta != 0.0f) {
+                const float4 x = *reinterpret_cast<const float4*>(o);
+                v.x = fmaf(beta, x.x, v.x);
+                v.y = fmaf(beta, x.y, v.y);
+                v.z = fmaf(beta, x.z, v.z);
+                v.w = fmaf(beta, x.w, v.w);
+            }
+            *reinterpret_cast<float4*>(o) = v;
+        } else {
+            for (int e = 0; e < 4 && c + e < cols; ++e) {
+                float a = w[e];
+                for (int s = 1; s < S; ++s)
+                    a += w[s * slice + e];
+                float v = alpha * a;
+                if (beta != 0.0f)
+                    v = fmaf(beta, o[e], v);
+                o[e] = v;
+            }
         }
-        float4 o = make_float4(alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w);
-        if (beta != 0.0f) {
-            const float4 c = reinterpret_cast<const float4*>(C)[i];
-            o.x = fmaf(beta, c.x, o.x);
-            o.y = fmaf(beta, c.y, o.y);
-            o.z = fmaf(beta, c.z, o.z);
-            o.w = fmaf(beta, c.w, o.w);
-        }
-        reinterpret_cast<float4*>(C)[i] = o;
-    }
-    for (long long i = 4 * n4 + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-        float a = ws[i];
-        for (int s = 1; s < S; ++s)
-            a += ws[s * slice + i];
-        float o = alpha * a;
-        if (beta != 0.0f)
-            o = fmaf(beta, C[i], o);
-        C[i] = o;
     }
 }
 
-cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long n, float alpha,
-                                 float beta, int sm_count, cudaStream_t stream)
+cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long rows, long long cols,
+                                 long long ldc, float alpha, float beta, int sm_count, cudaStream_t stream)
 {
-    if (n <= 0)
+    if (rows <= 0 || cols <= 0)
         return cudaSuccess;
-    long long blocks = (n / 4 + 255) / 256;
+    long long blocks = (rows * ((cols + 3) / 4) + 255) / 256;
     const long long cap = 8LL * (sm_count > 0 ? sm_count : 1);
     if (blocks > cap)
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    sat_splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, S, slice, C, n, alpha, beta);
+    sat_splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, S, slice, C, rows, cols, ldc,
+                                                                               alpha, beta);
     return cudaGetLastError();
 }
 

@@ -14,12 +14,17 @@ constexpr int kDtFP16 = 2;
 constexpr int kProdTMA = 0;    // TMA tensor loads (16-byte aligned bases and strides)
 constexpr int kProdPlain = 1;  // plain loads into the same swizzled layout (any stride)
 constexpr int kProdSwap = 2;   // TMA loads, operand roles exchanged: the MMA computes C^T = B^T A^T
+constexpr int kProdTN = 3;     // TMA loads, A stored transposed (K x M): first operand MN-major
+constexpr int kProdNT = 4;     // TMA loads, B stored transposed (N x K): second operand K-major
+constexpr int kProdTT = 5;     // TMA loads, both stored transposed
 
 struct GemmArgs {
     int M, N, K;
     const void* A;             // M x K row-major (plain-load producer only)
     const void* B;             // K x N row-major (plain-load producer only)
     float* C;                  // output: C (M x N), or the split-K workspace (splits x out_rows x N)
+    int64_t lda, ldb;          // row strides of A and B in elements (plain-load producer only)
+    int64_t ldc;               // row stride of the output the kernel writes, in floats
     float alpha, beta;
     int tiles_m, tiles_n;      // tiles of (128 * cta_group) x BN
     int num_tiles;             // work units: tiles_m * tiles_n * splits

@@ -50,6 +50,14 @@ struct Traits {
     // contiguous, K-major). For skinny M, where 128-row tiles of C would be
     // mostly empty.
     static constexpr bool SWAP = PROD == kProdSwap;
+    // Operand layouts in shared memory: the first MMA operand (the
+    // accumulator's rows) MN-major when it comes from a matrix stored with
+    // those rows contiguous (A stored K x M, or B for a swapped tile), else
+    // K-major; the second (its columns) K-major when it comes from a matrix
+    // stored with K contiguous (B stored N x K, or A for a swapped tile),
+    // else MN-major.
+    static constexpr bool A_MN = SWAP || PROD == kProdTN || PROD == kProdTT;
+    static constexpr bool B_KM = SWAP || PROD == kProdNT || PROD == kProdTT;
     static constexpr bool kTF32 = DT == kDtTF32;
     static constexpr int ES = kTF32 ? 4 : 2;        // bytes per operand element
     static constexpr int BM = 128;                  // accumulator rows per CTA
@@ -60,8 +68,8 @@ struct Traits {
     static constexpr int BN_CTA = BN / CG;          // B columns this CTA loads
     static constexpr int NBOX = BN_CTA / CW;        // B boxes per stage
     static constexpr int A_BYTES = BM * 128;
-    static constexpr int NBOX_A = BM / CW;          // swapped: boxes of CW columns n of B per stage
-    static constexpr int B_BYTES = SWAP ? BN * 128 : NBOX * BK * 128;
+    static constexpr int NBOX_A = BM / CW;          // MN-major first operand: boxes of CW rows per stage
+    static constexpr int B_BYTES = BN_CTA * 128;    // either layout: BN_CTA x BK elements
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // Epilogue: 8 warps (4 with the plain-load producer), two (one) per TMEM
     // lane quarter, taking alternate 32-column chunks. Each has one 4 KB staging buffer: 32 rows x 128
@@ -96,7 +104,7 @@ struct Traits {
     // producer of tf32 instead stores B transposed, K-major like A.
     static constexpr bool B_MN = true;
     static constexpr uint32_t B_LAYOUT = kTF32 ? kLayoutSW128Atom32 : kLayoutSW128;
-    static constexpr uint32_t IDESC = SWAP ? idesc_f32acc(FMT, BM, BN, false, true) : idesc_f32acc(FMT, BM * CG, BN, B_MN);
+    static constexpr uint32_t IDESC = idesc_f32acc(FMT, BM * CG, BN, !B_KM, A_MN);
     // MN-major: 128-byte column blocks are BK*128 bytes apart (leading byte
     // offset); K rows come in swizzle groups, 8 rows (1024 bytes) for the
     // 16-byte-atom swizzle and 4 rows (512 bytes) for the 32-byte-atom one
@@ -108,7 +116,9 @@ struct Traits {
     static constexpr uint32_t B_KSTEP = B_MN ? UK * 128 : UK * ES;
     static constexpr uint32_t A_KSTEP = UK * ES;    // bytes per MMA step of K in A (= 32)
 
-    static_assert(SWAP || BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
+    static_assert(B_KM || BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
+    static_assert(!B_KM || BN_CTA % 8 == 0, "K-major tile: whole 8-row swizzle groups");
+    static_assert(BK == CW, "one 128-byte row of K per stage");
     static_assert(!SWAP || (CG == 1 && BN >= 32), "swapped tiles: 1-SM, whole 32-column chunks");
     static_assert(BN >= 16 && BN <= 256 && BN % 16 == 0, "MMA N");
     static_assert(STAGES >= 2, "ring too small");
@@ -346,34 +356,39 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         }
                         const uint32_t fb = full0 + 8u * stage;
                         const int k0 = kb * T::BK;
-                        if constexpr (T::SWAP) {
-                            // First operand: columns m0 .. m0 + 127 of B (the
-                            // tile's rows are columns of C), NBOX_A boxes of CW
-                            // columns; second: rows n0 .. n0 + BN - 1 of A.
-                            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
+                        // The first operand (this CTA's 128 accumulator rows
+                        // from m0) and the second (its BN_CTA columns from n0),
+                        // each as it lies in memory: K-major as one box of
+                        // BK x rows, MN-major as boxes of CW rows x BK. A
+                        // swapped tile reads the first from B, the second from A.
+                        const CUtensorMap* t1 = T::SWAP ? &tmB : &tmA;
+                        const CUtensorMap* t2 = T::SWAP ? &tmA : &tmB;
+                        auto load = [&](uint32_t dst, const CUtensorMap* t, int x, int y) {
+                            if constexpr (CG == 1)
+                                tma_load_2d(dst, t, fb, x, y);
+                            else
+                                tma_load_2d_pair(dst, t, fb, x, y);
+                        };
+                        // In a pair only the leader arms the barrier, for both
+                        // CTAs' bytes; the peer's copies just complete on it. A
+                        // peer copy landing first drives the transaction count
+                        // negative, which the barrier allows, and the leader's
+                        // pending arrival keeps the phase open.
+                        if (CG == 1 || leader)
+                            mbar_arrive_expect_tx(full_bar(stage), CG * T::STAGE_BYTES);
+                        if constexpr (T::A_MN) {
 #pragma unroll
                             for (int j = 0; j < T::NBOX_A; ++j)
-                                tma_load_2d(sA + stage * T::A_BYTES + j * (T::BK * 128), &tmB, fb, m0 + j * T::CW, k0);
-                            tma_load_2d(sB + stage * T::B_BYTES, &tmA, fb, k0, n0);
-                        } else if constexpr (CG == 1) {
-                            mbar_arrive_expect_tx(fb, T::STAGE_BYTES);
-                            tma_load_2d(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
-#pragma unroll
-                            for (int j = 0; j < T::NBOX; ++j)
-                                tma_load_2d(sB + stage * T::B_BYTES + j * (T::BK * 128), &tmB, fb, n0 + j * T::CW, k0);
+                                load(sA + stage * T::A_BYTES + j * (T::BK * 128), t1, m0 + j * T::CW, k0);
                         } else {
-                            // Only the leader arms the barrier, for both CTAs'
-                            // bytes; the peer's copies just complete on it. A
-                            // peer copy landing first drives the transaction
-                            // count negative, which the barrier allows, and the
-                            // leader's pending arrival keeps the phase open.
-                            if (leader)
-                                mbar_arrive_expect_tx(full_bar(stage), 2 * T::STAGE_BYTES);
-                            tma_load_2d_pair(sA + stage * T::A_BYTES, &tmA, fb, k0, m0);
+                            load(sA + stage * T::A_BYTES, t1, k0, m0);
+                        }
+                        if constexpr (T::B_KM) {
+                            load(sB + stage * T::B_BYTES, t2, k0, n0);
+                        } else {
 #pragma unroll
                             for (int j = 0; j < T::NBOX; ++j)
-                                tma_load_2d_pair(sB + stage * T::B_BYTES + j * (T::BK * 128), &tmB, fb,
-                                                 n0 + j * T::CW, k0);
+                                load(sB + stage * T::B_BYTES + j * (T::BK * 128), t2, n0 + j * T::CW, k0);
                         }
                         if (++stage == T::STAGES) {
                             stage = 0;
@@ -460,7 +475,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         const int r = ar0 + 4 * i;
                         const int gr = m0 + r;
                         const bool v = gk < args.K && gr < args.M;
-                        const uint32_t* src = v ? gA + static_cast<int64_t>(gr) * args.K + gk : gA;
+                        const uint32_t* src = v ? gA + static_cast<int64_t>(gr) * args.lda + gk : gA;
                         cp_async_4(dA + static_cast<uint32_t>(r * 128 + ((((ak >> 2) ^ (r & 7)) << 4) | ((ak & 3) << 2))),
                                    src, v ? 4u : 0u);
                     }
@@ -474,7 +489,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                         for (int kr = 0; kr < T::BK; ++kr) {
                             const int gk2 = k0 + kr;
                             const bool v = gn < args.N && gk2 < args.K;
-                            const uint32_t* src = v ? gB + static_cast<int64_t>(gk2) * args.N + gn : gB;
+                            const uint32_t* src = v ? gB + static_cast<int64_t>(gk2) * args.ldb + gn : gB;
                             cp_async_4(col + static_cast<uint32_t>(kr * 128 + ((((nn >> 3) ^ (kr & 3)) << 5))), src,
                                        v ? 4u : 0u);
                         }
@@ -543,7 +558,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             const int idx = p + (i0 + i) * NP;
                             const int r = idx / T::BK, k = idx - r * T::BK;
                             const int gm = m0 + r, gk = k0 + k;
-                            v[i] = (gm < args.M && gk < args.K) ? __ldg(gA + static_cast<int64_t>(gm) * args.K + gk)
+                            v[i] = (gm < args.M && gk < args.K) ? __ldg(gA + static_cast<int64_t>(gm) * args.lda + gk)
                                                                 : E(0);
                         }
 #pragma unroll
@@ -564,7 +579,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                             const int idx = p + (i0 + i) * NP;
                             const int kr = idx / BN, n = idx - kr * BN;
                             const int gk = k0 + kr, gn = n0 + n;
-                            v[i] = (gk < args.K && gn < args.N) ? __ldg(gB + static_cast<int64_t>(gk) * args.N + gn)
+                            v[i] = (gk < args.K && gn < args.N) ? __ldg(gB + static_cast<int64_t>(gk) * args.ldb + gn)
                                                                 : E(0);
                         }
 #pragma unroll
@@ -624,11 +639,12 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     const uint32_t b0 = sB + stage * T::B_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < T::KSTEPS; ++ks) {
-                        // Swapped: the first operand is MN-major (laid out as
-                        // B is otherwise), the second K-major (as A is).
-                        const uint64_t ad = T::SWAP ? sdesc(a0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT)
+                        // K-major operands: 128-byte rows, one MMA step of K
+                        // 32 bytes on; MN-major: column blocks BK*128 bytes
+                        // apart, one MMA step of K UK rows on.
+                        const uint64_t ad = T::A_MN ? sdesc(a0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT)
                                                     : sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
-                        const uint64_t bd = T::SWAP ? sdesc(b0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128)
+                        const uint64_t bd = T::B_KM ? sdesc(b0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128)
                                                     : sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
                         mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb != w.kb0 || ks != 0) ? 1u : 0u);
                     }
@@ -684,7 +700,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         const float alpha = args.alpha, beta = args.beta;
-        const int64_t ldc = args.N;
+        const int64_t ldc = args.ldc;
         constexpr int NCHUNK = BN / 32;
         // C values (bulk-store path, beta != 0) of row (row0 + lane), columns
         // gcol0 .. gcol0 + 31, as 8 aligned float4 loads; zero outside M x N.

@@ -80,6 +80,8 @@ constexpr KernelEntry make_entry()
                        T::B_LAYOUT == kLayoutSW128Atom32 ? static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)
                                                          : static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B),
                        T::C_RING_OK ? 1 : 0,
+                       T::A_MN ? 1 : 0,
+                       T::B_KM ? 1 : 0,
                        &prepare_variant<DT, BN, CG, PROD>, &max_clusters_variant<DT, BN, CG, PROD>,
                        &launch_variant<DT, BN, CG, PROD>};
 }
@@ -89,6 +91,9 @@ constexpr KernelEntry make_entry()
     make_entry<DT, 64, 1, kProdTMA>(), make_entry<DT, 128, 1, kProdTMA>(), make_entry<DT, 256, 1, kProdTMA>(), \
         make_entry<DT, 128, 2, kProdTMA>(), make_entry<DT, 256, 2, kProdTMA>(),                                 \
         make_entry<DT, 128, 1, kProdPlain>(), make_entry<DT, 256, 1, kProdPlain>(),                             \
-        make_entry<DT, 32, 1, kProdSwap>(), make_entry<DT, 64, 1, kProdSwap>(), make_entry<DT, 128, 1, kProdSwap>()
+        make_entry<DT, 32, 1, kProdSwap>(), make_entry<DT, 64, 1, kProdSwap>(), make_entry<DT, 128, 1, kProdSwap>(), \
+        make_entry<DT, 128, 1, kProdTN>(), make_entry<DT, 256, 1, kProdTN>(), make_entry<DT, 256, 2, kProdTN>(),    \
+        make_entry<DT, 128, 1, kProdNT>(), make_entry<DT, 256, 1, kProdNT>(), make_entry<DT, 256, 2, kProdNT>(),    \
+        make_entry<DT, 128, 1, kProdTT>(), make_entry<DT, 256, 1, kProdTT>(), make_entry<DT, 256, 2, kProdTT>()
 
 }  // namespace sat

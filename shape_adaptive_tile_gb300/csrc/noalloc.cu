@@ -172,7 +172,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
         return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (K == 0 || alpha == 0.0f) {
-        e = sat::launch_scale(C, static_cast<long long>(M * N), beta, stream);
+        e = sat::launch_scale(C, M, N, N, beta, stream);
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_LAUNCH, "beta-scale kernel: %s", cudaGetErrorString(e));
     }
     if (!A || !B)
@@ -240,6 +240,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     a.K = static_cast<int>(K);
     a.A = A;
     a.B = B;
+    a.lda = K;
+    a.ldb = N;
+    a.ldc = N;
     a.C = splits > 1 ? ws : C;
     a.alpha = splits > 1 ? 1.0f : alpha;
     a.beta = splits > 1 ? 0.0f : beta;
@@ -287,8 +290,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     if (e != cudaSuccess)
         return fail(GEMM_ERR_LAUNCH, "launching the GEMM kernel: %s", cudaGetErrorString(e));
     if (splits > 1) {
-        e = sat::launch_splitk_reduce(ws, splits, static_cast<long long>(ws_rows) * N, C,
-                                      static_cast<long long>(M * N), alpha, beta, ds->sm_count, stream);
+        e = sat::launch_splitk_reduce(ws, splits, static_cast<long long>(ws_rows) * N, C, M, N, N, alpha, beta,
+                                      ds->sm_count, stream);
         if (e != cudaSuccess)
             return fail(GEMM_ERR_LAUNCH, "launching the split-K reduction: %s", cudaGetErrorString(e));
     }

@@ -20,6 +20,8 @@ struct KernelEntry {
     int bk;        // K per stage
     int b_swizzle; // CUtensorMapSwizzle of B's tensor map
     int c_ring;    // 1: with beta != 0 the producer can fetch C through the operand ring
+    int a_mn;      // 1: the first MMA operand is read MN-major (A stored K x M, or B for a swapped tile)
+    int b_km;      // 1: the second MMA operand is read K-major (B stored N x K, or A for a swapped tile)
     cudaError_t (*prepare)();  // sets the kernel's dynamic shared-memory limit
     int (*max_clusters)();     // co-resident CTA pairs on this device (cg == 2), 0 if unknown
     cudaError_t (*launch)(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
@@ -50,10 +52,10 @@ inline void tile_grid(const KernelEntry* e, int64_t M, int64_t N, int64_t* tiles
     *tiles_n = (cols + e->bn - 1) / e->bn;
 }
 
-// Defined in aux_kernels.cu.
-cudaError_t launch_scale(float* C, long long n, float beta, cudaStream_t stream);
+// Defined in aux_kernels.cu. C is rows x cols floats with row stride ldc.
+cudaError_t launch_scale(float* C, long long rows, long long cols, long long ldc, float beta, cudaStream_t stream);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
-cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long n, float alpha,
-                                 float beta, int sm_count, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long rows, long long cols,
+                                 long long ldc, float alpha, float beta, int sm_count, cudaStream_t stream);
 
 }  // namespace sat
