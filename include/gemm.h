@@ -51,6 +51,13 @@ typedef enum {
 
 typedef struct gemm_plan gemm_plan; /* opaque */
 
+/* Element type of C for gemm_plan_create_ex (accumulation is fp32 either way). */
+typedef enum {
+    GEMM_C_F32 = 0,  /* fp32 */
+    GEMM_C_BF16 = 1, /* bfloat16, rounded to nearest even */
+    GEMM_C_F16 = 2   /* IEEE binary16, rounded to nearest even */
+} gemm_ctype_t;
+
 /*
  * Choose the kernel (tile shape, CTA-pair or single SM, stage count, raster
  * order, load path) for this problem on the CURRENT device, and prepare it.
@@ -88,6 +95,10 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
  * As gemm_plan_create_config, for C = alpha * op(A) * op(B) + beta * C where
  * op(A) is M x K and op(B) is K x N: trans_a != 0 means A is stored as its
  * transpose (K x M, row-major), trans_b != 0 that B is (N x K, row-major).
+ * c_type gives C's element type: with GEMM_C_BF16 or GEMM_C_F16 the
+ * epilogue reads C (beta != 0) and writes it in that type, computing
+ * alpha * acc + beta * C in fp32 and rounding once to nearest even; such C
+ * is written row by row (no bulk-store epilogue, no C through the ring).
  * Transposed operands are read by TMA only (no plain-load kernel exists for
  * them), so every gemm_run_ex of such a plan needs A and B 16-byte aligned
  * with row strides that are multiples of 16 bytes (GEMM_ERR_ALIGN
@@ -96,7 +107,7 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
  * is rounded to one of these, and ",swap" is ignored. `config` may be NULL.
  */
 gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int trans_a, int trans_b,
-                               const char* config);
+                               gemm_ctype_t c_type, const char* config);
 
 /*
  * Enqueue C = alpha * A * B + beta * C on `cuda_stream` (a cudaStream_t; NULL
@@ -126,13 +137,14 @@ int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, floa
 /*
  * gemm_run with row strides (leading dimensions, in elements): lda for A as
  * stored (>= K, or >= M when the plan has A transposed), ldb for B as stored
- * (>= N, or >= K when transposed), ldc for C (>= N, in floats). gemm_run is
- * this call with the dense strides. Operands whose row strides are not
+ * (>= N, or >= K when transposed), ldc for C (>= N, in elements of the
+ * plan's C type; C points to elements of that type, aligned to their size).
+ * gemm_run is this call with the dense strides. Operands whose row strides are not
  * 16-byte multiples take the plain-load path (untransposed plans only); C
  * whose row stride is not a 16-byte multiple takes the row-store epilogue.
  * GEMM_ERR_ARG for a stride below the minimum.
  */
-int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                 float alpha, float beta, void* cuda_stream);
 
 /*

@@ -52,7 +52,7 @@ def lib() -> ctypes.CDLL:
             L.gemm_plan_create_config.restype = vp
             L.gemm_run.argtypes = [vp, vp, vp, vp, f32, f32, vp]
             L.gemm_run.restype = i32
-            L.gemm_plan_create_ex.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.c_char_p]
+            L.gemm_plan_create_ex.argtypes = [i64, i64, i64, i32, i32, i32, i32, ctypes.c_char_p]
             L.gemm_plan_create_ex.restype = vp
             L.gemm_run_ex.argtypes = [vp, vp, i64, vp, i64, vp, i64, f32, f32, vp]
             L.gemm_run_ex.restype = i32
@@ -104,8 +104,13 @@ def gemm_plan_create_config(M: int, N: int, K: int, dtype, config: str | None) -
     return h
 
 
-def gemm_plan_create_ex(M: int, N: int, K: int, dtype, trans_a: bool, trans_b: bool, config: str | None = None) -> int:
+C_TYPES = {"fp32": 0, "bf16": 1, "fp16": 2}
+
+
+def gemm_plan_create_ex(M: int, N: int, K: int, dtype, trans_a: bool, trans_b: bool, c_type="fp32",
+                        config: str | None = None) -> int:
     h = lib().gemm_plan_create_ex(M, N, K, _dt(dtype), int(bool(trans_a)), int(bool(trans_b)),
+                                  C_TYPES[c_type] if isinstance(c_type, str) else int(c_type),
                                   config.encode() if config else None)
     if not h:
         raise GemmError(-1, gemm_last_error())
@@ -163,11 +168,11 @@ class Plan:
     """Owns one gemm_plan; ``run`` takes device tensors (or raw pointers)."""
 
     def __init__(self, M: int, N: int, K: int, dtype, config: str | None = None, trans_a: bool = False,
-                 trans_b: bool = False):
+                 trans_b: bool = False, c_type="fp32"):
         self.M, self.N, self.K, self.dtype = M, N, K, dtype
         self.trans_a, self.trans_b = trans_a, trans_b
-        if trans_a or trans_b:
-            self.handle = gemm_plan_create_ex(M, N, K, dtype, trans_a, trans_b, config)
+        if trans_a or trans_b or c_type not in ("fp32", 0):
+            self.handle = gemm_plan_create_ex(M, N, K, dtype, trans_a, trans_b, c_type, config)
         else:
             self.handle = gemm_plan_create_config(M, N, K, dtype, config)
 

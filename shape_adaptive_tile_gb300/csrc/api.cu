@@ -97,6 +97,7 @@ struct gemm_plan {
     int device = 0;
     int sm_count = 0;
     bool trans_a = false, trans_b = false;  // A stored K x M, B stored N x K
+    int c_half = 0;                         // element type of C: 0 fp32, 1 bf16, 2 fp16
     sat::Choice choice{};
     bool force_plain = false;
     bool c_ring = false;  // beta != 0: the producer fetches C through the operand ring
@@ -152,8 +153,12 @@ int grid_for(const gemm_plan* p, const sat::KernelEntry* e)
 }
 
 gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const char* config, bool trans_a = false,
-                  bool trans_b = false)
+                  bool trans_b = false, int c_type = 0)
 {
+    if (c_type < 0 || c_type > 2) {
+        fail(GEMM_ERR_ARG, "unknown C type %d", c_type);
+        return nullptr;
+    }
     g_err[0] = '\0';
     const int dt = static_cast<int>(dtype);
     if (M < 0 || N < 0 || K < 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) {
@@ -195,6 +200,7 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     p->sm_count = sms;
     p->trans_a = trans_a;
     p->trans_b = trans_b;
+    p->c_half = c_type;
     const int64_t es = elem_size(dt);
     // Dense row strides that TMA can describe. Transposed operands are read
     // by TMA only, so their plans assume it (gemm_run_ex checks each call).
@@ -338,7 +344,7 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
     const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
-    p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1 && p->sk_tiles == 0;
+    p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1 && p->sk_tiles == 0 && p->c_half == 0;
     char sk_desc[48] = "";
     if (p->sk_tiles)
         std::snprintf(sk_desc, sizeof sk_desc, " sk%d/%d", p->sk_tiles, p->sk_w);
@@ -347,6 +353,9 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
                   p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
                   source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "",
                   trans_a ? " ta" : "", trans_b ? " tb" : "");
+    if (c_type)
+        std::snprintf(p->desc + std::strlen(p->desc), sizeof p->desc - std::strlen(p->desc), " c%s",
+                      c_type == 1 ? "bf16" : "fp16");
     return p;
 }
 
@@ -354,9 +363,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
 
 namespace {
 
-int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, void* Cv, int64_t ldc,
              float alpha, float beta, void* cuda_stream)
 {
+    float* C = static_cast<float*>(Cv);  // fp32, or 16-bit elements when the plan's C type says so
     if (!p)
         return fail(GEMM_ERR_ARG, "plan is NULL");
     if (p->M == 0 || p->N == 0)
@@ -366,8 +376,8 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
                     (long long)ldb, (long long)ldc);
     if (!C)
         return fail(GEMM_ERR_ARG, "C is NULL");
-    if (reinterpret_cast<uintptr_t>(C) % 4 != 0)
-        return fail(GEMM_ERR_ALIGN, "C must be 4-byte aligned");
+    if (reinterpret_cast<uintptr_t>(C) % (p->c_half ? 2 : 4) != 0)
+        return fail(GEMM_ERR_ALIGN, "C must be aligned to its element size");
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -376,7 +386,7 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         return fail(GEMM_ERR_ARG, "plan was made for device %d but device %d is current", p->device, dev);
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (p->K == 0 || alpha == 0.0f) {
-        e = sat::launch_scale(C, p->M, p->N, ldc, beta, stream);
+        e = sat::launch_scale(C, p->c_half, p->M, p->N, ldc, beta, stream);
         return e == cudaSuccess ? GEMM_OK : cuda_fail(e, "launching the beta-scale kernel");
     }
     if (!A || !B)
@@ -404,6 +414,7 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     a.lda = lda;
     a.ldb = ldb;
     a.ldc = ldc;
+    a.c_half = p->c_half;
     a.alpha = alpha;
     a.beta = beta;
     int64_t tiles_m = 0, tiles_n = 0;
@@ -421,6 +432,7 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         // reduction applies alpha and beta.
         a.C = p->ws;
         a.ldc = p->N;
+        a.c_half = 0;
         a.alpha = 1.0f;
         a.beta = 0.0f;
         a.out_rows = p->ws_rows;
@@ -432,8 +444,9 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
 
     // C goes through the bulk-store epilogue when its base and row stride
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
-    const bool c_tma =
-        split ? p->ws_tma : p->N % 4 == 0 && ldc % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+    // (16-bit C always goes through the row-store epilogue.)
+    const bool c_tma = split ? p->ws_tma
+                             : p->c_half == 0 && p->N % 4 == 0 && ldc % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
     if (use_tma && p->sk_tiles > 0) {
@@ -508,8 +521,8 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the GEMM kernel");
     if (split) {
-        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->M, p->N,
-                                      ldc, alpha, beta, p->sm_count, stream);
+        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->c_half, p->M,
+                                      p->N, ldc, alpha, beta, p->sm_count, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the split-K reduction");
     }
@@ -531,9 +544,9 @@ gemm_plan* gemm_plan_create_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t
 }
 
 gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int trans_a, int trans_b,
-                               const char* config)
+                               gemm_ctype_t c_type, const char* config)
 {
-    return create(M, N, K, dtype, config, trans_a != 0, trans_b != 0);
+    return create(M, N, K, dtype, config, trans_a != 0, trans_b != 0, static_cast<int>(c_type));
 }
 
 void gemm_plan_destroy(gemm_plan* plan)
@@ -563,7 +576,7 @@ int gemm_run(const gemm_plan* p, const void* A, const void* B, float* C, float a
     return run_impl(p, A, p->trans_a ? p->M : p->K, B, p->trans_b ? p->K : p->N, C, p->N, alpha, beta, cuda_stream);
 }
 
-int gemm_run_ex(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+int gemm_run_ex(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                 float alpha, float beta, void* cuda_stream)
 {
     return run_impl(p, A, lda, B, ldb, C, ldc, alpha, beta, cuda_stream);

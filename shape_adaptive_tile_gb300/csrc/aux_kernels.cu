@@ -7,21 +7,24 @@
 
 namespace sat {
 
-__global__ void sat_scale_kernel(float* __restrict__ C, long long rows, long long cols, long long ldc, float beta)
+__global__ void sat_scale_kernel(float* __restrict__ C, int kind, long long rows, long long cols, long long ldc,
+                                 float beta)
 {
     for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
-        float* row = C + r * ldc;
-        for (long long c = threadIdx.x; c < cols; c += blockDim.x)
-            row[c] = beta == 0.0f ? 0.0f : beta * row[c];
+        for (long long c = threadIdx.x; c < cols; c += blockDim.x) {
+            const long long i = r * ldc + c;
+            c_store(C, kind, i, beta == 0.0f ? 0.0f : beta * c_load(C, kind, i));
+        }
     }
 }
 
-cudaError_t launch_scale(float* C, long long rows, long long cols, long long ldc, float beta, cudaStream_t stream)
+cudaError_t launch_scale(float* C, int kind, long long rows, long long cols, long long ldc, float beta,
+                         cudaStream_t stream)
 {
     if (rows <= 0 || cols <= 0)
         return cudaSuccess;
     const long long blocks = rows < 8192 ? rows : 8192;
-    sat_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, rows, cols, ldc, beta);
+    sat_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, kind, rows, cols, ldc, beta);
     return cudaGetLastError();
 }
 
@@ -32,17 +35,18 @@ cudaError_t launch_scale(float* C, long long rows, long long cols, long long ldc
 // reads C. Memory-bound: S + 1 (+1) floats of traffic per output element.
 // Each thread takes four consecutive columns of one row, as one 16-byte
 // access where the columns, the strides and C allow it.
-__global__ void sat_splitk_reduce_kernel(const float* __restrict__ ws, int S, long long slice, float* C,
+__global__ void sat_splitk_reduce_kernel(const float* __restrict__ ws, int S, long long slice, float* C, int kind,
                                          long long rows, long long cols, long long ldc, float alpha, float beta)
 {
     const long long c4 = (cols + 3) / 4;
-    const bool vec = cols % 4 == 0 && ldc % 4 == 0 && slice % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+    const bool vec = kind == 0 && cols % 4 == 0 && ldc % 4 == 0 && slice % 4 == 0 &&
+                     reinterpret_cast<uintptr_t>(C) % 16 == 0;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * c4; i += stride) {
         const long long r = i / c4, c = (i - r * c4) * 4;
         const float* w = ws + r * cols + c;
-        float* o = C + r * ldc + c;
         if (vec) {
+            float* o = C + r * ldc + c;
             float4 a = *reinterpret_cast<const float4*>(w);
             for (int s = 1; s < S; ++s) {
                 const float4 b = *reinterpret_cast<const float4*>(w + s * slice);
@@ -66,16 +70,18 @@ __global__ void sat_splitk_reduce_kernel(const float* __restrict__ ws, int S, lo
                 for (int s = 1; s < S; ++s)
                     a += w[s * slice + e];
                 float v = alpha * a;
+                const long long i = r * ldc + c + e;
                 if (beta != 0.0f)
-                    v = fmaf(beta, o[e], v);
-                o[e] = v;
+                    v = fmaf(beta, c_load(C, kind, i), v);
+                c_store(C, kind, i, v);
             }
         }
     }
 }
 
-cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long rows, long long cols,
-                                 long long ldc, float alpha, float beta, int sm_count, cudaStream_t stream)
+cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, int kind, long long rows,
+                                 long long cols, long long ldc, float alpha, float beta, int sm_count,
+                                 cudaStream_t stream)
 {
     if (rows <= 0 || cols <= 0)
         return cudaSuccess;
@@ -85,8 +91,8 @@ cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float*
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
-    sat_splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, S, slice, C, rows, cols, ldc,
-                                                                               alpha, beta);
+    sat_splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, S, slice, C, kind, rows, cols,
+                                                                               ldc, alpha, beta);
     return cudaGetLastError();
 }
 

@@ -24,7 +24,8 @@ struct GemmArgs {
     const void* B;             // K x N row-major (plain-load producer only)
     float* C;                  // output: C (M x N), or the split-K workspace (splits x out_rows x N)
     int64_t lda, ldb;          // row strides of A and B in elements (plain-load producer only)
-    int64_t ldc;               // row stride of the output the kernel writes, in floats
+    int64_t ldc;               // row stride of the output the kernel writes, in elements
+    int c_half;                // element type of C: 0 fp32, 1 bf16, 2 fp16 (16-bit C: row-store epilogue only)
     float alpha, beta;
     int tiles_m, tiles_n;      // tiles of (128 * cta_group) x BN
     int num_tiles;             // work units: tiles_m * tiles_n * splits

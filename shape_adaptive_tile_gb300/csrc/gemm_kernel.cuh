@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             ct[j] = beta != 0.0f && crow + j < args.M && ccol < args.N
-                                        ? args.C[static_cast<int64_t>(crow + j) * ldc + ccol]
+                                        ? c_load(args.C, args.c_half, static_cast<int64_t>(crow + j) * ldc + ccol)
                                         : 0.0f;
                         if (args.c_tma) {
                             // Stage the 32 x 32 block of C (rows crow.., columns
@@ -875,7 +875,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                                 bulk_commit();
                             }
                         } else if (ccol < args.N) {
-                            float* cp = args.C + (static_cast<int64_t>(yoff) + crow) * ldc + ccol;
+                            const int64_t c0 = (static_cast<int64_t>(yoff) + crow) * ldc + ccol;
                             const int rows = min(32, args.M - crow);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                                     float v = alpha * __uint_as_float(r[j]);
                                     if (beta != 0.0f)
                                         v = fmaf(beta, ct[j], v);
-                                    cp[j * ldc] = v;
+                                    c_store(args.C, args.c_half, c0 + j * ldc, v);
                                 }
                             }
                         }
@@ -966,14 +966,15 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
                     __syncwarp();
                     const int col = gcol0 + lane;
                     if (col < args.N) {
-                        float* cp = args.C + (static_cast<int64_t>(yoff) + row0) * ldc + col;
+                        const int64_t c0 = (static_cast<int64_t>(yoff) + row0) * ldc + col;
                         const int rows = min(32, args.M - row0);
+                        const int kind = args.c_half;
 #pragma unroll 4
                         for (int i = 0; i < rows; ++i) {
                             float v = alpha * buf[i * 32 + (lane ^ i)];
                             if (beta != 0.0f)
-                                v = fmaf(beta, cp[i * ldc], v);
-                            cp[i * ldc] = v;
+                                v = fmaf(beta, c_load(args.C, kind, c0 + i * ldc), v);
+                            c_store(args.C, kind, c0 + i * ldc, v);
                         }
                     }
                     __syncwarp();

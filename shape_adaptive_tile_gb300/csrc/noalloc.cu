@@ -172,7 +172,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
         return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (K == 0 || alpha == 0.0f) {
-        e = sat::launch_scale(C, M, N, N, beta, stream);
+        e = sat::launch_scale(C, 0, M, N, N, beta, stream);
         return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_LAUNCH, "beta-scale kernel: %s", cudaGetErrorString(e));
     }
     if (!A || !B)
@@ -290,7 +290,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     if (e != cudaSuccess)
         return fail(GEMM_ERR_LAUNCH, "launching the GEMM kernel: %s", cudaGetErrorString(e));
     if (splits > 1) {
-        e = sat::launch_splitk_reduce(ws, splits, static_cast<long long>(ws_rows) * N, C, M, N, N, alpha, beta,
+        e = sat::launch_splitk_reduce(ws, splits, static_cast<long long>(ws_rows) * N, C, 0, M, N, N, alpha, beta,
                                       ds->sm_count, stream);
         if (e != cudaSuccess)
             return fail(GEMM_ERR_LAUNCH, "launching the split-K reduction: %s", cudaGetErrorString(e));

@@ -5,6 +5,8 @@
 // library.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 #include <cuda.h>
 
@@ -271,6 +273,27 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
 {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
+}
+
+// Element idx of C stored as fp32 (kind 0), bf16 (1) or fp16 (2); 16-bit
+// stores round to nearest even.
+__device__ __forceinline__ float c_load(const float* C, int kind, int64_t idx)
+{
+    if (kind == 1)
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(C)[idx]);
+    if (kind == 2)
+        return __half2float(reinterpret_cast<const __half*>(C)[idx]);
+    return C[idx];
+}
+
+__device__ __forceinline__ void c_store(float* C, int kind, int64_t idx, float v)
+{
+    if (kind == 1)
+        reinterpret_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+    else if (kind == 2)
+        reinterpret_cast<__half*>(C)[idx] = __float2half_rn(v);
+    else
+        C[idx] = v;
 }
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float a)

@@ -52,10 +52,13 @@ inline void tile_grid(const KernelEntry* e, int64_t M, int64_t N, int64_t* tiles
     *tiles_n = (cols + e->bn - 1) / e->bn;
 }
 
-// Defined in aux_kernels.cu. C is rows x cols floats with row stride ldc.
-cudaError_t launch_scale(float* C, long long rows, long long cols, long long ldc, float beta, cudaStream_t stream);
+// Defined in aux_kernels.cu. C is rows x cols elements with row stride ldc,
+// of kind 0 (fp32), 1 (bf16) or 2 (fp16).
+cudaError_t launch_scale(float* C, int kind, long long rows, long long cols, long long ldc, float beta,
+                         cudaStream_t stream);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
-cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, long long rows, long long cols,
-                                 long long ldc, float alpha, float beta, int sm_count, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, int kind, long long rows,
+                                 long long cols, long long ldc, float alpha, float beta, int sm_count,
+                                 cudaStream_t stream);
 
 }  // namespace sat

@@ -131,3 +131,47 @@ def test_k_zero_scales_strided_c():
     out = dC.cpu().numpy()
     assert np.array_equal(out[:, :N], (0.25 * C0.astype(np.float64)).astype(np.float32))
     assert np.all(out[:, N:] == SENTINEL)
+
+
+def _c16(x, c_type):
+    """fp32 values rounded to the 16-bit C type (nearest, ties to even), as bit patterns."""
+    if c_type == "bf16":
+        return si.f32_to_bf16_bits(x.astype(np.float32))
+    return x.astype(np.float32).astype(np.float16).view(np.uint16)
+
+
+# 16-bit C: the epilogue reads C in that type (beta != 0), computes in fp32
+# and rounds once. Dyadic C0 is exact in both 16-bit types; the fp32 result
+# is exact, so rounding it once must give the oracle's value rounded once.
+@pytest.mark.parametrize("config", [None, "256,2,0,4", "128,1,1,2,3", "64,1,0,4,swap"])
+@pytest.mark.parametrize("c_type", ["bf16", "fp16"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_16_bit_c_dyadic(dtype, c_type, config):
+    M, N, K = 333, 520, 264
+    if config and "swap" in config:
+        M = 27
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 81, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    ldc = N + 8
+    Cs = np.full((M, ldc), 0x1234, np.uint16)
+    Cs[:, :N] = _c16(C0, c_type)
+    dC = torch.from_numpy(Cs).cuda()
+    with sat.Plan(M, N, K, dtype, config, c_type=c_type) as plan:
+        desc = plan.describe()
+        assert f" c{c_type}" in desc
+        plan.run(to_dev(A, dtype), to_dev(B, dtype), dC, 1.5, 0.5, stream(), ldc=ldc)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    out = dC.cpu().numpy()
+    assert np.all(out[:, N:] == 0x1234), f"C padding was written [{desc}]"
+    assert np.array_equal(out[:, :N], _c16(ref32, c_type)), f"{dtype} -> {c_type} [{desc}]"
+
+
+def test_16_bit_c_with_k_zero_scales_in_place():
+    M, N = 20, 30
+    C0 = si.c_matrix("dyadic", M, N, 5)
+    dC = torch.from_numpy(_c16(C0, "bf16")).cuda()
+    with sat.Plan(M, N, 0, "bf16", c_type="bf16") as plan:
+        plan.run(0, 0, dC, 1.0, 0.5, stream())
+        torch.cuda.synchronize()
+    assert np.array_equal(dC.cpu().numpy(), _c16(0.5 * C0, "bf16"))
