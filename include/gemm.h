@@ -223,6 +223,20 @@ const char* gemm_last_error(void);
 int gemm_selftest_bounded_wait(uint64_t timeout_ns);
 
 /*
+ * The GEMM as a device routine inside a kernel of the library's own: the
+ * routine (sat::gemm_cta in gemm_kernel.cuh, callable by any kernel that
+ * meets the conditions stated there) computes C = alpha * A * B + beta * C
+ * as phase 1 of a persistent kernel, whose phase 2, in the same launch,
+ * replaces each element of the tiles the CTA produced by max(x, 0). Dense
+ * row-major operands, 16-byte aligned with 16-byte-multiple row strides
+ * (GEMM_ERR_ALIGN otherwise); 1-SM 128 x 128 tiles; no error word, so a
+ * bounded wait that gives up shows only in the result. For tests: it shows
+ * that the routine composes with other work in one launch.
+ */
+int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const void* A, const void* B,
+                              float* C, float alpha, float beta, void* cuda_stream);
+
+/*
  * Host-only view of the dispatcher (no device is touched): the choice that
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row

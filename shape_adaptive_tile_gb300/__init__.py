@@ -25,7 +25,7 @@ STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_ARG", -2: "GEMM_ERR_ARCH", -3: "GEMM_ERR_A
 # Every function the C ABI exports (include/gemm.h).
 EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_plan_create_ex", "gemm_run", "gemm_run_ex",
            "gemm_run_host", "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
-           "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc")
+           "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc", "gemm_selftest_device_call")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.gemm_selftest_bounded_wait.argtypes = [ctypes.c_uint64]
             L.gemm_selftest_bounded_wait.restype = i32
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
+            L.gemm_selftest_device_call.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
+            L.gemm_selftest_device_call.restype = i32
             L.gemm_run_noalloc.restype = i32
             L.gemm_select_config.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.c_char_p, i32]
             L.gemm_select_config.restype = i32
@@ -134,6 +136,12 @@ def gemm_run_noalloc(M: int, N: int, K: int, dtype, A, B, C, alpha: float = 1.0,
                      stream=None) -> int:
     """The allocation-free GEMM (see include/gemm.h): no plan, fixed scratch."""
     return lib().gemm_run_noalloc(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, _p(stream))
+
+
+def gemm_selftest_device_call(M: int, N: int, K: int, dtype, A, B, C, alpha: float = 1.0, beta: float = 0.0,
+                              stream=None) -> int:
+    """GEMM then ReLU in one launch, the GEMM being the device-callable routine (see include/gemm.h)."""
+    return lib().gemm_selftest_device_call(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, _p(stream))
 
 
 def gemm_plan_destroy(plan: int) -> None:

@@ -22,8 +22,8 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libsatgemm.so")
 STAMP = os.path.join(LIB_DIR, "libsatgemm.stamp")
 
-SOURCES = ["api.cu", "aux_kernels.cu", "dispatch.cpp", "kernels_tf32.cu", "kernels_bf16.cu", "kernels_fp16.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "aux_kernels.cu", "dispatch.cpp", "tensor_map.cpp", "kernels_tf32.cu", "kernels_bf16.cu",
+           "kernels_fp16.cu", "noalloc.cu", "device_call.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

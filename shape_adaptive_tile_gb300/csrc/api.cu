@@ -31,25 +31,6 @@ int fail(int code, const char* fmt, ...)
     return code;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 int elem_size(int dt) { return dt == sat::kDtTF32 ? 4 : 2; }
 
 const char* dt_name(int dt) { return dt == 0 ? "tf32" : dt == 1 ? "bf16" : "fp16"; }
@@ -59,21 +40,15 @@ const char* dt_name(int dt) { return dt == 0 ? "tf32" : dt == 1 ? "bf16" : "fp16
 int encode_2d(CUtensorMap* map, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer, CUtensorMapSwizzle swizzle, uint64_t ld = 0)
 {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn)
-        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available from the driver");
     const CUtensorMapDataType t = dt == sat::kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                   : dt == sat::kDtBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {(ld ? ld : inner) * static_cast<uint64_t>(elem_size(dt))};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    const int r = sat::encode_map(map, t, elem_size(dt), ptr, inner, outer, ld ? ld : inner, box_inner, box_outer,
+                                  swizzle);
+    if (r == -1)
+        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled is not available from the driver");
+    if (r != 0)
+        return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", r);
     return 0;
 }
 

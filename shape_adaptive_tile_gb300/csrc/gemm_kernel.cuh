@@ -233,13 +233,26 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
            ((((nb >> 4) ^ static_cast<uint32_t>(k & 7)) << 4) | (nb & 15u));
 }
 
+// The GEMM of `args`, as a device routine: the part of the persistent tile
+// schedule that falls to this CTA (CTAs blockIdx.x of gridDim.x, in pairs for
+// CG == 2). Any kernel can call it once, with all of its threads, as one phase
+// of a longer (persistent) kernel, provided that:
+//   - the block has Traits::THREADS threads and at least Traits::SMEM_BYTES
+//     of dynamic shared memory at smem_raw (the routine aligns it to 1024
+//     bytes itself), and no other use of that shared memory overlaps the call;
+//   - for CG == 2 the grid is launched in clusters of 2;
+//   - every CTA of the grid calls it (the schedule spans the whole grid), and
+//     for stream-K layouts all of the grid is resident at once;
+//   - tmA, tmB, tmC are tensor maps in parameter, constant or global memory,
+//     encoded as the host entry points encode them.
+// On return the CTA's share of C is written; bulk stores are complete, and
+// the CTA's tensor memory is freed. The routine's own work is all inside
+// the call: nothing is left pending for the caller.
 template <int DT, int BN, int CG, int PROD>
-__global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
-    sat_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+__device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                         const GemmArgs& args, uint8_t* smem_raw)
 {
     using T = Traits<DT, BN, CG, PROD>;
-    extern __shared__ uint8_t smem_raw[];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1011,8 +1024,10 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         } else {
             tile_loop(Plain{});
         }
-        if (args.c_tma && lane == 0)
+        if (args.c_tma && lane == 0) {
             bulk_wait<0>();  // every bulk store of this warp has completed
+            fence_proxy_async_global();
+        }
         __syncwarp();
     }
 
@@ -1025,6 +1040,15 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
         tc_fence_after();
         tmem_dealloc<CG>(tmem_base, T::TMEM_COLS);
     }
+}
+
+template <int DT, int BN, int CG, int PROD>
+__global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
+    sat_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    gemm_cta<DT, BN, CG, PROD>(tmA, tmB, tmC, args, smem_raw);
 }
 
 }  // namespace sat

@@ -57,38 +57,11 @@ int fail(int code, const char* fmt, ...)
     return code;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 // Row-major 2-D tensor map, 128-byte-swizzled boxes, zero fill outside.
 bool encode(CUtensorMap* map, CUtensorMapDataType t, int es, const void* ptr, uint64_t inner, uint64_t outer,
             uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
 {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn)
-        return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * static_cast<uint64_t>(es)};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return sat::encode_map(map, t, es, ptr, inner, outer, inner, box_inner, box_outer, swz) == 0;
 }
 
 // First call on a device, with that device current: look up where the

@@ -198,6 +198,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's async-proxy global accesses (bulk stores) with its
+// later generic ones.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- cp.async (non-bulk asynchronous copies) ---------------------------------
 
 // Copy 4 bytes global -> shared without passing through registers; with

@@ -39,6 +39,14 @@ extern const int kNumEntriesFP16;
 // Sets the message gemm_last_error() returns on this thread (api.cu).
 void set_last_error(const char* msg);
 
+// Encodes a 2-D tensor map of a row-major matrix: `outer` rows of `inner`
+// elements, `ld` elements apart, read or written in boxes of box_inner x
+// box_outer with the given swizzle and zero fill outside the matrix.
+// Returns 0, -1 if the driver's encoder is unavailable, or the driver's
+// error code (tensor_map.cpp).
+int encode_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const void* ptr, uint64_t inner,
+               uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
 // Finds the variant, or nullptr.
 const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
 

@@ -186,6 +186,21 @@ def test_swapped_operands_with_c_not_16_byte_aligned():
     checks.assert_bit_exact(flatC[1:].view(M, N).cpu().numpy(), ref32, "swapped, C misaligned")
 
 
+# The GEMM as a device routine: phase 1 of a kernel whose phase 2 (same
+# launch) applies max(x, 0) to the tiles each CTA produced. 48 tiles (one
+# per CTA) and 176 tiles (more than the SMs: the persistent loop).
+@pytest.mark.parametrize("M,N,K", [(700, 1000, 520), (2000, 1400, 264)])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_device_callable_gemm_inside_a_megakernel(dtype, M, N, K):
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 91, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, dtype)
+    dC = to_dev(C0)
+    assert sat.gemm_selftest_device_call(M, N, K, dtype, to_dev(A, dtype), to_dev(B, dtype), dC, 1.5, -0.5,
+                                         stream()) == 0, sat.gemm_last_error()
+    torch.cuda.synchronize()
+    checks.assert_bit_exact(dC.cpu().numpy(), np.maximum(ref32, np.float32(0)), f"{dtype} {M}x{N}x{K} fused relu")
+
+
 def test_k_zero_and_alpha_zero_scale_c():
     M, N = 70, 90
     C0 = si.c_matrix("normal", M, N, 3)
