@@ -1,4 +1,5 @@
-"""Python face of the FP64 CPU GEMM oracle (``gemm_oracle.c``).
+"""Python face of the FP64 CPU oracles: GEMM (``gemm_oracle.c``) and the
+row operators softmax, RMSNorm and LayerNorm (``rowops.c``).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package; the library
@@ -21,7 +22,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_SRCS = [os.path.join(_HERE, "gemm_oracle.c"), os.path.join(_HERE, "rowops.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle.so")
 _CODES = {"tf32": 0, "fp32": 0, "bf16": 1, "fp16": 2}
@@ -38,13 +39,13 @@ def build(force: bool = False) -> str:
     never leaves an old one in place.
     """
     os.makedirs(_BUILD, exist_ok=True)
-    fresh = os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)
+    fresh = os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS)
     if fresh and not force:
         return _LIB
     if os.path.exists(_LIB):
         os.remove(_LIB)
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", *CFLAGS, "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -64,6 +65,12 @@ def _load():
             lib.oracle_decode.restype = ctypes.c_double
             lib.oracle_threads.argtypes = []
             lib.oracle_threads.restype = ctypes.c_int
+            lib.oracle_softmax_rows.argtypes = [p, i64, i64, i64, p]
+            lib.oracle_softmax_rows.restype = None
+            lib.oracle_rmsnorm_rows.argtypes = [p, i64, p, i64, i64, d, p]
+            lib.oracle_rmsnorm_rows.restype = None
+            lib.oracle_layernorm_rows.argtypes = [p, i64, p, p, i64, i64, d, p]
+            lib.oracle_layernorm_rows.restype = None
             _lib = lib
     return _lib
 
@@ -157,3 +164,50 @@ def rel_rms(c, ref64) -> float:
     if den == 0.0:
         return 0.0 if num == 0.0 else float("inf")
     return num / den
+
+
+# ---- row operators (rowops.c) ---------------------------------------------------
+
+
+def _rows_in(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim != 2:
+        raise ValueError("x must be rows x width")
+    return x
+
+
+def _vec(v, width):
+    if v is None:
+        return None
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    if v.shape != (width,):
+        raise ValueError("gamma/beta must have one entry per column")
+    return v
+
+
+def softmax(x):
+    """Row-wise softmax of fp32 x (rows x width), in double."""
+    x = _rows_in(x)
+    y = np.empty(x.shape, np.float64)
+    _load().oracle_softmax_rows(_ptr(x), x.shape[1], x.shape[0], x.shape[1], _ptr(y))
+    return y
+
+
+def rmsnorm(x, gamma=None, eps=1e-5):
+    """Row-wise RMSNorm of fp32 x with optional per-column gamma, in double."""
+    x = _rows_in(x)
+    g = _vec(gamma, x.shape[1])
+    y = np.empty(x.shape, np.float64)
+    _load().oracle_rmsnorm_rows(_ptr(x), x.shape[1], _ptr(g) if g is not None else None, x.shape[0], x.shape[1],
+                                float(eps), _ptr(y))
+    return y
+
+
+def layernorm(x, gamma=None, beta=None, eps=1e-5):
+    """Row-wise LayerNorm (biased variance) of fp32 x with optional gamma and beta, in double."""
+    x = _rows_in(x)
+    g, b = _vec(gamma, x.shape[1]), _vec(beta, x.shape[1])
+    y = np.empty(x.shape, np.float64)
+    _load().oracle_layernorm_rows(_ptr(x), x.shape[1], _ptr(g) if g is not None else None,
+                                  _ptr(b) if b is not None else None, x.shape[0], x.shape[1], float(eps), _ptr(y))
+    return y
