@@ -17,6 +17,7 @@ gemm_run_host from pinned host buffers, copies included.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference      # the FP64 CPU oracle on host cores
   python bench.py --all results.json    # every workload, one line each (not the driver line)
+  python bench.py --rowops results.json # the row operators (softmax, RMSNorm, LayerNorm), GB/s
 Under torchrun every rank runs its own replica (the GEMM has no exchange
 step); the line reports the whole job.
 """
@@ -233,6 +234,46 @@ def traffic_for(desc):
     return None
 
 
+def bench_rowops(args, torch, sat):
+    """Each row operator at each rows x width of the pages: median of the
+    timed steps (CUDA events, L2 flushed before each), against the HBM roof
+    of 8 bytes per element (one read, one write)."""
+    pk, _ = peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    out = []
+    for rows, width in si.ROWOP_SHAPES:
+        x, g, b = si.rowop_inputs(rows, width)
+        dx, dg, db = (torch.from_numpy(v).to(dev) for v in (x, g, b))
+        dy = torch.empty_like(dx)
+        calls = {
+            "softmax": lambda: sat.rowop_softmax(dx, width, dy, width, rows, width, stream.cuda_stream),
+            "rmsnorm": lambda: sat.rowop_rmsnorm(dx, width, dg, dy, width, rows, width, 1e-5, stream.cuda_stream),
+            "layernorm": lambda: sat.rowop_layernorm(dx, width, dg, db, dy, width, rows, width, 1e-5,
+                                                     stream.cuda_stream),
+        }
+        for op in si.ROWOPS:
+            for _ in range(args.warmup):
+                sat.check(calls[op]())
+            times = []
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                sat.check(calls[op]())
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            med = statistics.median(times)
+            gbs = 8.0 * rows * width / (med * 1e-3) / 1e9
+            item = {"op": op, "rows": rows, "width": width, "median_us": med * 1e3, "min_us": min(times) * 1e3,
+                    "samples": len(times), "gb_per_s": gbs, "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
+            out.append(item)
+            print(json.dumps(item), flush=True)
+    return out
+
+
 def bench_one(args, w, rank, world, torch, sat, quiet=False):
     name, dt, (M, N, K), fam, alpha, beta, cfam, seed, _ = w
     A, B, C0 = si.problem(M, N, K, dt, fam, seed, cfam)
@@ -325,6 +366,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(workloads()))
     ap.add_argument("--all", metavar="JSON", help="bench every workload and write per-workload results")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rowops", metavar="JSON", help="bench the row operators and write per-case results")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -348,6 +390,13 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     sat.lib()
+
+    if args.rowops:
+        out = bench_rowops(args, torch, sat)
+        if rank == 0:
+            with open(args.rowops, "w") as f:
+                json.dump(out, f, indent=1)
+        return 0
 
     if args.all:
         out = []

@@ -25,7 +25,8 @@ STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_ARG", -2: "GEMM_ERR_ARCH", -3: "GEMM_ERR_A
 # Every function the C ABI exports (include/gemm.h).
 EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_plan_create_ex", "gemm_run", "gemm_run_ex",
            "gemm_run_host", "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
-           "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc", "gemm_selftest_device_call")
+           "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc", "gemm_selftest_device_call",
+           "rowop_softmax", "rowop_rmsnorm", "rowop_layernorm")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +72,12 @@ def lib() -> ctypes.CDLL:
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
             L.gemm_selftest_device_call.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
             L.gemm_selftest_device_call.restype = i32
+            L.rowop_softmax.argtypes = [vp, i64, vp, i64, i64, i64, vp]
+            L.rowop_softmax.restype = i32
+            L.rowop_rmsnorm.argtypes = [vp, i64, vp, vp, i64, i64, i64, f32, vp]
+            L.rowop_rmsnorm.restype = i32
+            L.rowop_layernorm.argtypes = [vp, i64, vp, vp, vp, i64, i64, i64, f32, vp]
+            L.rowop_layernorm.restype = i32
             L.gemm_run_noalloc.restype = i32
             L.gemm_select_config.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.c_char_p, i32]
             L.gemm_select_config.restype = i32
@@ -142,6 +149,22 @@ def gemm_selftest_device_call(M: int, N: int, K: int, dtype, A, B, C, alpha: flo
                               stream=None) -> int:
     """GEMM then ReLU in one launch, the GEMM being the device-callable routine (see include/gemm.h)."""
     return lib().gemm_selftest_device_call(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, _p(stream))
+
+
+# ---- row operators (include/rowops.h) -----------------------------------------
+
+
+def rowop_softmax(X, ldx: int, Y, ldy: int, rows: int, width: int, stream=None) -> int:
+    return lib().rowop_softmax(_p(X), ldx, _p(Y), ldy, rows, width, _p(stream))
+
+
+def rowop_rmsnorm(X, ldx: int, gamma, Y, ldy: int, rows: int, width: int, eps: float = 1e-5, stream=None) -> int:
+    return lib().rowop_rmsnorm(_p(X), ldx, _p(gamma), _p(Y), ldy, rows, width, eps, _p(stream))
+
+
+def rowop_layernorm(X, ldx: int, gamma, beta, Y, ldy: int, rows: int, width: int, eps: float = 1e-5,
+                    stream=None) -> int:
+    return lib().rowop_layernorm(_p(X), ldx, _p(gamma), _p(beta), _p(Y), ldy, rows, width, eps, _p(stream))
 
 
 def gemm_plan_destroy(plan: int) -> None:

@@ -23,7 +23,7 @@ LIB = os.path.join(LIB_DIR, "libsatgemm.so")
 STAMP = os.path.join(LIB_DIR, "libsatgemm.stamp")
 
 SOURCES = ["api.cu", "aux_kernels.cu", "dispatch.cpp", "tensor_map.cpp", "kernels_tf32.cu", "kernels_bf16.cu",
-           "kernels_fp16.cu", "noalloc.cu", "device_call.cu"]
+           "kernels_fp16.cu", "noalloc.cu", "device_call.cu", "rowops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -37,7 +37,7 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
-    files.append(os.path.join(INCLUDE, "gemm.h"))
+    files += [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h")]
     return [f for f in files if os.path.isfile(f)]
 
 

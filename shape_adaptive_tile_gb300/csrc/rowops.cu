@@ -1,0 +1,235 @@
+// Row operators over a rows x width fp32 matrix: softmax, RMSNorm and
+// LayerNorm of each row (include/rowops.h).
+//
+// These are the wide-row reductions of "Scale coverage exposes a remaining
+// GEMM gap" (section "Reductions: wide rows and large working sets"),
+// 37 x 8191 to 16384 x 4096. They read each element once and write it once,
+// so HBM bandwidth bounds them: 8 bytes per element. One CTA of 512 threads
+// takes a row; each thread keeps its PER elements of the row in registers
+// between the reductions and the write, so the row is read from memory once.
+// Loads are 16 bytes wide where the row start, the row strides and the width
+// allow it, 4 bytes otherwise; consecutive threads read consecutive
+// addresses either way. Reductions go warp by warp with shuffles, then
+// across the 16 warps through shared memory, in a fixed order: the result
+// is the same on every run.
+#include "rowops.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "registry.h"
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+enum Op { kSoftmax = 0, kRMSNorm = 1, kLayerNorm = 2 };
+
+// Sum (or maximum) over the block, the same value returned to every thread.
+template <bool kMax>
+__device__ __forceinline__ float block_reduce(float v, float* scratch)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float u = __shfl_xor_sync(0xffffffffu, v, o);
+        v = kMax ? fmaxf(v, u) : v + u;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // the scratch of an earlier reduction has been read
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    float t = lane < kWarps ? scratch[lane] : (kMax ? -INFINITY : 0.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float u = __shfl_xor_sync(0xffffffffu, t, o);
+        t = kMax ? fmaxf(t, u) : t + u;
+    }
+    return t;
+}
+
+// Element e of this thread's share: column e * kThreads * VEC + threadIdx.x * VEC
+// + (lane within the vector). VEC = 4 loads 16 bytes at a time.
+template <int OP, int PER, int VEC>
+__global__ void __launch_bounds__(kThreads)
+    sat_rowop_kernel(const float* X, int64_t ldx, const float* __restrict__ gamma,
+                     const float* __restrict__ beta, float* Y, int64_t ldy, int64_t rows, int width,
+                     float eps)
+{
+    __shared__ float scratch[kWarps];
+    constexpr int NV = PER / VEC;  // vectors per thread
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float* x = X + r * ldx;
+        float v[PER];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = (i * kThreads + threadIdx.x) * VEC;
+            if constexpr (VEC == 4) {
+                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < width)
+                    q = *reinterpret_cast<const float4*>(x + c);
+                v[4 * i] = q.x;
+                v[4 * i + 1] = q.y;
+                v[4 * i + 2] = q.z;
+                v[4 * i + 3] = q.w;
+            } else {
+                v[i] = c < width ? x[c] : 0.0f;
+            }
+        }
+        auto valid = [&](int i) { return (i / VEC * kThreads + threadIdx.x) * VEC + i % VEC < width; };
+        float scale = 0.0f, shift = 0.0f;
+        if constexpr (OP == kSoftmax) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                if (valid(i))
+                    m = fmaxf(m, v[i]);
+            m = block_reduce<true>(m, scratch);
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                v[i] = valid(i) ? expf(v[i] - m) : 0.0f;
+                s += v[i];
+            }
+            s = block_reduce<false>(s, scratch);
+            scale = 1.0f / s;
+        } else if constexpr (OP == kRMSNorm) {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                s = fmaf(v[i], v[i], s);  // padding entries are zero
+            s = block_reduce<false>(s, scratch);
+            scale = 1.0f / sqrtf(s / static_cast<float>(width) + eps);
+        } else {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                s += v[i];
+            shift = block_reduce<false>(s, scratch) / static_cast<float>(width);
+            float q = 0.0f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const float d = valid(i) ? v[i] - shift : 0.0f;
+                q = fmaf(d, d, q);
+            }
+            q = block_reduce<false>(q, scratch);
+            scale = 1.0f / sqrtf(q / static_cast<float>(width) + eps);
+        }
+        float* y = Y + r * ldy;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = (i * kThreads + threadIdx.x) * VEC;
+            if (c >= width)
+                continue;
+            float o[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float t = v[VEC * i + e];
+                if constexpr (OP == kSoftmax) {
+                    o[e] = t * scale;
+                } else {
+                    const float g = gamma ? gamma[c + e] : 1.0f;
+                    o[e] = OP == kRMSNorm ? t * scale * g
+                                          : fmaf((t - shift) * scale, g, beta ? beta[c + e] : 0.0f);
+                }
+            }
+            if constexpr (VEC == 4)
+                *reinterpret_cast<float4*>(y + c) = make_float4(o[0], o[1], o[2], o[3]);
+            else
+                y[c] = o[0];
+        }
+    }
+}
+
+int fail(int code, const char* fmt, ...)
+{
+    char msg[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(msg, sizeof msg, fmt, ap);
+    va_end(ap);
+    sat::set_last_error(msg);
+    return code;
+}
+
+template <int OP, int PER, int VEC>
+cudaError_t launch_one(const float* X, int64_t ldx, const float* gamma, const float* beta, float* Y, int64_t ldy,
+                       int64_t rows, int width, float eps, cudaStream_t stream)
+{
+    const int64_t grid = rows < 65535 ? rows : 65535;
+    sat_rowop_kernel<OP, PER, VEC><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(X, ldx, gamma, beta, Y, ldy,
+                                                                                        rows, width, eps);
+    return cudaGetLastError();
+}
+
+template <int OP, int VEC>
+cudaError_t launch_vec(const float* X, int64_t ldx, const float* g, const float* b, float* Y, int64_t ldy,
+                       int64_t rows, int width, float eps, cudaStream_t s)
+{
+    // The smallest register share that holds the row.
+    if (width <= kThreads * 4)
+        return launch_one<OP, 4, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= kThreads * 8)
+        return launch_one<OP, 8, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= kThreads * 16)
+        return launch_one<OP, 16, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= kThreads * 32)
+        return launch_one<OP, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    return launch_one<OP, 64, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+}
+
+template <int OP>
+int run(const float* X, int64_t ldx, const float* gamma, const float* beta, float* Y, int64_t ldy, int64_t rows,
+        int64_t width, float eps, void* stream)
+{
+    sat::set_last_error("");
+    if (rows < 0 || width < 0)
+        return fail(GEMM_ERR_ARG, "negative size");
+    if (rows == 0 || width == 0)
+        return GEMM_OK;
+    if (width > kRowopMaxWidth)
+        return fail(GEMM_ERR_ARG, "width %lld is above the %d these kernels hold in registers", (long long)width,
+                    kRowopMaxWidth);
+    if (!X || !Y)
+        return fail(GEMM_ERR_ARG, "X or Y is NULL");
+    if (ldx < width || ldy < width)
+        return fail(GEMM_ERR_ARG, "row stride below the width");
+    if (reinterpret_cast<uintptr_t>(X) % 4 || reinterpret_cast<uintptr_t>(Y) % 4 ||
+        (gamma && reinterpret_cast<uintptr_t>(gamma) % 4) || (beta && reinterpret_cast<uintptr_t>(beta) % 4))
+        return fail(GEMM_ERR_ALIGN, "operands must be 4-byte aligned");
+    auto al16 = [](const void* p) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    const bool vec = width % 4 == 0 && ldx % 4 == 0 && ldy % 4 == 0 && al16(X) && al16(Y) && al16(gamma) &&
+                     al16(beta);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int w = static_cast<int>(width);
+    const cudaError_t e = vec ? launch_vec<OP, 4>(X, ldx, gamma, beta, Y, ldy, rows, w, eps, s)
+                              : launch_vec<OP, 1>(X, ldx, gamma, beta, Y, ldy, rows, w, eps, s);
+    return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_LAUNCH, "launching the row kernel: %s", cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int rowop_softmax(const float* X, int64_t ldx, float* Y, int64_t ldy, int64_t rows, int64_t width, void* stream)
+{
+    return run<kSoftmax>(X, ldx, nullptr, nullptr, Y, ldy, rows, width, 0.0f, stream);
+}
+
+int rowop_rmsnorm(const float* X, int64_t ldx, const float* gamma, float* Y, int64_t ldy, int64_t rows, int64_t width,
+                  float eps, void* stream)
+{
+    return run<kRMSNorm>(X, ldx, gamma, nullptr, Y, ldy, rows, width, eps, stream);
+}
+
+int rowop_layernorm(const float* X, int64_t ldx, const float* gamma, const float* beta, float* Y, int64_t ldy,
+                    int64_t rows, int64_t width, float eps, void* stream)
+{
+    return run<kLayerNorm>(X, ldx, gamma, beta, Y, ldy, rows, width, eps, stream);
+}
+
+}  // extern "C"

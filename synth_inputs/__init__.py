@@ -175,5 +175,22 @@ WORKLOADS = [
                       (128, 8192, 8192), (4096, 4096, 512))
 ]
 
+# The row-operator workloads: rows x width of the wide-row softmax, RMSNorm
+# and LayerNorm cases ("Scale coverage exposes a remaining GEMM gap",
+# section "Reductions: wide rows and large working sets"), fp32.
+ROWOP_SHAPES = [(37, 8191), (1024, 8192), (1024, 16384), (4096, 8192), (8192, 4096), (16384, 4096)]
+ROWOPS = ("softmax", "rmsnorm", "layernorm")
+
+
+def rowop_inputs(rows: int, width: int, seed: int = 6):
+    """X ~ N(0,1) (rows x width), gamma = 1 + U(-1/2, 1/2) and beta ~ N(0, 1/4)
+    per column, all fp32. The pages give no distribution; these keep every
+    operator's output of order one."""
+    x = matrix("normal", "tf32", rows, width, seed, 0)
+    gamma = (1.0 + 0.5 * matrix("uniform", "tf32", 1, width, seed, 1)[0].astype(np.float64)).astype(np.float32)
+    beta = (0.5 * matrix("normal", "tf32", 1, width, seed, 2)[0].astype(np.float64)).astype(np.float32)
+    return x, gamma, beta
+
+
 # rel_rms bounds per dtype (the deterministic-GEMM acceptance gates).
 REL_RMS_BOUND = {"tf32": 1e-3, "bf16": 8e-3, "fp16": 8e-3}

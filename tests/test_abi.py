@@ -1,6 +1,7 @@
 """The C-ABI library without a GPU: it builds for sm_103a, loads, exports
-every function include/gemm.h declares, fails cleanly when no device is
-present, and its dispatcher (host logic only) makes sane choices."""
+every function include/gemm.h and include/rowops.h declare, fails cleanly
+when no device is present, and its dispatcher (host logic only) makes sane
+choices."""
 import ctypes
 import os
 import re
@@ -9,7 +10,8 @@ import pytest
 
 import shape_adaptive_tile_gb300 as sat
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,14 +21,15 @@ def lib():
 
 
 def _declared():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:gemm|rowop)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for fn in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_last_error", "gemm_plan_describe"):
+    for fn in ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_last_error", "gemm_plan_describe",
+               "rowop_softmax", "rowop_rmsnorm", "rowop_layernorm"):
         assert fn in names
 
 

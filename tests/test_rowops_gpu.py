@@ -1,0 +1,143 @@
+"""GPU parity of the row operators (softmax, RMSNorm, LayerNorm) against the
+FP64 oracle, through the C ABI, at every rows x width the pages time.
+
+Tolerances follow from fp32 arithmetic: each output is a handful of
+rounded operations (exp to 2 ulp, one division or square root) on top of a
+sum of at most 32 terms per thread and a 9-level tree across threads, so
+its relative error stays below about 3e-6 for N(0,1) rows. The gates are:
+softmax max |y - ref| / ref <= 1e-5; the norms max |y - ref| / (|ref| + 1)
+<= 1e-5. The largest shapes are compared on 256 sampled rows (the oracle
+runs on just those rows); the rest in full. Two runs give the same bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shape_adaptive_tile_gb300 as sat
+import synth_inputs as si
+from tests.gpu_util import stream
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    sat.build()
+    sat.lib()
+
+
+_cache = {}
+
+
+def _inputs(rows, width):
+    if (rows, width) not in _cache:
+        _cache.clear()
+        _cache[(rows, width)] = si.rowop_inputs(rows, width)
+    return _cache[(rows, width)]
+
+
+def _device_run(op, x, g, b, ldx=None, ldy=None, y=None):
+    rows, width = x.shape[0], x.shape[1] if ldx is None else x.shape[1]
+    dx = x if isinstance(x, torch.Tensor) else torch.from_numpy(x).cuda()
+    dy = torch.empty_like(dx) if y is None else y
+    ldx = dx.shape[1] if ldx is None else ldx
+    ldy = dy.shape[1] if ldy is None else ldy
+    width = dx.shape[1] if width is None else width
+    dg = torch.from_numpy(g).cuda() if g is not None else None
+    db = torch.from_numpy(b).cuda() if b is not None else None
+    if op == "softmax":
+        rc = sat.rowop_softmax(dx, ldx, dy, ldy, rows, width, stream())
+    elif op == "rmsnorm":
+        rc = sat.rowop_rmsnorm(dx, ldx, dg, dy, ldy, rows, width, 1e-5, stream())
+    else:
+        rc = sat.rowop_layernorm(dx, ldx, dg, db, dy, ldy, rows, width, 1e-5, stream())
+    assert rc == 0, sat.gemm_last_error()
+    torch.cuda.synchronize()
+    return dy
+
+
+def _reference(op, x, g, b):
+    if op == "softmax":
+        return oracle.softmax(x)
+    if op == "rmsnorm":
+        return oracle.rmsnorm(x, g)
+    return oracle.layernorm(x, g, b)
+
+
+def _check(op, got, ref, what):
+    got = got.astype(np.float64)
+    err = np.abs(got - ref) / (ref if op == "softmax" else np.abs(ref) + 1.0)
+    assert np.all(np.isfinite(got)), what
+    worst = float(err.max())
+    assert worst <= TOL, f"{what}: max relative error {worst:.3g} > {TOL}"
+
+
+@pytest.mark.parametrize("rows,width", si.ROWOP_SHAPES)
+@pytest.mark.parametrize("op", si.ROWOPS)
+def test_rowop_matches_oracle_and_repeats(op, rows, width):
+    x, g, b = _inputs(rows, width)
+    y1 = _device_run(op, x, g, b)
+    y2 = _device_run(op, x, g, b)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32)), "two runs differ"
+    got = y1.cpu().numpy()
+    if rows * width > 1024 * 16384:
+        sel = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(rows).integers(0, rows, 254)]))
+        _check(op, got[sel], _reference(op, x[sel], g, b), f"{op} {rows}x{width} (sampled rows)")
+    else:
+        _check(op, got, _reference(op, x, g, b), f"{op} {rows}x{width}")
+
+
+@pytest.mark.parametrize("op", si.ROWOPS)
+@pytest.mark.parametrize("width", [1, 3, 4, 513, 2048, 16385, 32768])
+def test_rowop_widths_and_tails(op, width):
+    x, g, b = si.rowop_inputs(5, width, seed=7)
+    got = _device_run(op, x, g, b).cpu().numpy()
+    _check(op, got, _reference(op, x, g, b), f"{op} width {width}")
+
+
+@pytest.mark.parametrize("op", si.ROWOPS)
+def test_rowop_strided_and_in_place(op):
+    rows, width = 9, 1000
+    x, g, b = si.rowop_inputs(rows, width, seed=8)
+    ref = _reference(op, x, g, b)
+    # strided: rows 1100 apart in X, 1024 apart in Y; padding must stay untouched
+    xs = np.full((rows, 1100), np.nan, np.float32)
+    xs[:, :width] = x
+    ys = torch.full((rows, 1024), -7.0, device="cuda")
+    dx = torch.from_numpy(xs).cuda()
+    if op == "softmax":
+        rc = sat.rowop_softmax(dx, 1100, ys, 1024, rows, width, stream())
+    elif op == "rmsnorm":
+        rc = sat.rowop_rmsnorm(dx, 1100, torch.from_numpy(g).cuda(), ys, 1024, rows, width, 1e-5, stream())
+    else:
+        rc = sat.rowop_layernorm(dx, 1100, torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda(), ys, 1024, rows,
+                                 width, 1e-5, stream())
+    assert rc == 0, sat.gemm_last_error()
+    torch.cuda.synchronize()
+    out = ys.cpu().numpy()
+    assert np.all(out[:, width:] == -7.0)
+    _check(op, out[:, :width], ref, f"{op} strided")
+    # in place
+    d = torch.from_numpy(x.copy()).cuda()
+    _device_run(op, d, g, b, y=d)
+    _check(op, d.cpu().numpy(), ref, f"{op} in place")
+
+
+def test_rowop_special_values_and_errors():
+    # softmax of one column is 1; LayerNorm of one column is beta; RMSNorm without gamma
+    x = np.array([[3.0], [-2.0]], np.float32)
+    assert np.all(_device_run("softmax", x, None, None).cpu().numpy() == 1.0)
+    b = np.array([0.25], np.float32)
+    assert np.all(_device_run("layernorm", x, np.array([2.0], np.float32), b).cpu().numpy() == 0.25)
+    got = _device_run("rmsnorm", np.full((2, 64), 2.0, np.float32), None, None).cpu().numpy()
+    assert np.allclose(got, 2.0 / np.sqrt(4.0 + 1e-5), rtol=1e-6)
+    dx = torch.zeros(4, 8, device="cuda")
+    assert sat.rowop_softmax(dx, 8, dx, 8, 0, 8, stream()) == 0           # no rows: nothing to do
+    assert sat.rowop_softmax(dx, 4, dx, 8, 4, 8, stream()) == -1          # stride below width
+    assert sat.rowop_softmax(None, 8, dx, 8, 4, 8, stream()) == -1
+    assert sat.rowop_rmsnorm(dx, 40000, None, dx, 40000, 1, 32769, 1e-5, stream()) == -1   # too wide
