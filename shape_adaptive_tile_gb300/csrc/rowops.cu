@@ -30,8 +30,11 @@ constexpr int kWarps = kThreads / 32;
 enum Op { kSoftmax = 0, kRMSNorm = 1, kLayerNorm = 2 };
 
 // Sum (or maximum) over the block, the same value returned to every thread.
+// Consecutive reductions alternate between two scratch rows, so one barrier
+// each suffices: a row is rewritten only two reductions later, after a
+// barrier that every thread passed after reading it.
 template <bool kMax>
-__device__ __forceinline__ float block_reduce(float v, float* scratch)
+__device__ __forceinline__ float block_reduce(float v, float (*scratch)[kWarps], int& turn)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -39,11 +42,12 @@ __device__ __forceinline__ float block_reduce(float v, float* scratch)
         v = kMax ? fmaxf(v, u) : v + u;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();  // the scratch of an earlier reduction has been read
+    float* row = scratch[turn];
+    turn ^= 1;
     if (lane == 0)
-        scratch[warp] = v;
+        row[warp] = v;
     __syncthreads();
-    float t = lane < kWarps ? scratch[lane] : (kMax ? -INFINITY : 0.0f);
+    float t = lane < kWarps ? row[lane] : (kMax ? -INFINITY : 0.0f);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float u = __shfl_xor_sync(0xffffffffu, t, o);
@@ -60,7 +64,8 @@ __global__ void __launch_bounds__(kThreads)
                      const float* __restrict__ beta, float* Y, int64_t ldy, int64_t rows, int width,
                      float eps)
 {
-    __shared__ float scratch[kWarps];
+    __shared__ float scratch[2][kWarps];
+    int turn = 0;
     constexpr int NV = PER / VEC;  // vectors per thread
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const float* x = X + r * ldx;
@@ -88,35 +93,35 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < PER; ++i)
                 if (valid(i))
                     m = fmaxf(m, v[i]);
-            m = block_reduce<true>(m, scratch);
+            m = block_reduce<true>(m, scratch, turn);
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 v[i] = valid(i) ? expf(v[i] - m) : 0.0f;
                 s += v[i];
             }
-            s = block_reduce<false>(s, scratch);
+            s = block_reduce<false>(s, scratch, turn);
             scale = 1.0f / s;
         } else if constexpr (OP == kRMSNorm) {
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < PER; ++i)
                 s = fmaf(v[i], v[i], s);  // padding entries are zero
-            s = block_reduce<false>(s, scratch);
+            s = block_reduce<false>(s, scratch, turn);
             scale = 1.0f / sqrtf(s / static_cast<float>(width) + eps);
         } else {
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < PER; ++i)
                 s += v[i];
-            shift = block_reduce<false>(s, scratch) / static_cast<float>(width);
+            shift = block_reduce<false>(s, scratch, turn) / static_cast<float>(width);
             float q = 0.0f;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const float d = valid(i) ? v[i] - shift : 0.0f;
                 q = fmaf(d, d, q);
             }
-            q = block_reduce<false>(q, scratch);
+            q = block_reduce<false>(q, scratch, turn);
             scale = 1.0f / sqrtf(q / static_cast<float>(width) + eps);
         }
         float* y = Y + r * ldy;
@@ -125,17 +130,41 @@ __global__ void __launch_bounds__(kThreads)
             const int c = (i * kThreads + threadIdx.x) * VEC;
             if (c >= width)
                 continue;
+            // gamma and beta for these VEC columns, 16 bytes at a time when VEC is 4
+            float gv[VEC], bv[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                gv[e] = 1.0f;
+                bv[e] = 0.0f;
+            }
+            if constexpr (OP != kSoftmax) {
+                if (gamma) {
+                    if constexpr (VEC == 4) {
+                        const float4 q = *reinterpret_cast<const float4*>(gamma + c);
+                        gv[0] = q.x, gv[1] = q.y, gv[2] = q.z, gv[3] = q.w;
+                    } else {
+                        gv[0] = gamma[c];
+                    }
+                }
+                if (OP == kLayerNorm && beta) {
+                    if constexpr (VEC == 4) {
+                        const float4 q = *reinterpret_cast<const float4*>(beta + c);
+                        bv[0] = q.x, bv[1] = q.y, bv[2] = q.z, bv[3] = q.w;
+                    } else {
+                        bv[0] = beta[c];
+                    }
+                }
+            }
             float o[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const float t = v[VEC * i + e];
-                if constexpr (OP == kSoftmax) {
+                if constexpr (OP == kSoftmax)
                     o[e] = t * scale;
-                } else {
-                    const float g = gamma ? gamma[c + e] : 1.0f;
-                    o[e] = OP == kRMSNorm ? t * scale * g
-                                          : fmaf((t - shift) * scale, g, beta ? beta[c + e] : 0.0f);
-                }
+                else if constexpr (OP == kRMSNorm)
+                    o[e] = t * scale * gv[e];
+                else
+                    o[e] = fmaf((t - shift) * scale, gv[e], bv[e]);
             }
             if constexpr (VEC == 4)
                 *reinterpret_cast<float4*>(y + c) = make_float4(o[0], o[1], o[2], o[3]);
