@@ -64,6 +64,15 @@ void set_last_error(const char* msg)
 {
     std::snprintf(g_err, sizeof g_err, "%s", msg);
 }
+
+int fail_with(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
 }  // namespace sat
 
 struct gemm_plan {
@@ -346,6 +355,8 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         return fail(GEMM_ERR_ARG, "plan is NULL");
     if (p->M == 0 || p->N == 0)
         return GEMM_OK;
+    if (lda >= (int64_t(1) << 31) || ldb >= (int64_t(1) << 31) || ldc >= (int64_t(1) << 31))
+        return fail(GEMM_ERR_ARG, "leading dimensions must be below 2^31");
     if ((p->K > 0 && (lda < (p->trans_a ? p->M : p->K) || ldb < (p->trans_b ? p->K : p->N))) || ldc < p->N)
         return fail(GEMM_ERR_ARG, "leading dimension too small (lda %lld, ldb %lld, ldc %lld)", (long long)lda,
                     (long long)ldb, (long long)ldc);
@@ -386,9 +397,9 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     a.A = A;
     a.B = B;
     a.C = C;
-    a.lda = lda;
-    a.ldb = ldb;
-    a.ldc = ldc;
+    a.lda = static_cast<int>(lda);
+    a.ldb = static_cast<int>(ldb);
+    a.ldc = static_cast<int>(ldc);
     a.c_half = p->c_half;
     a.alpha = alpha;
     a.beta = beta;
@@ -406,7 +417,7 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         // The GEMM writes raw fp32 partial tiles to the workspace; the
         // reduction applies alpha and beta.
         a.C = p->ws;
-        a.ldc = p->N;
+        a.ldc = static_cast<int>(p->N);
         a.c_half = 0;
         a.alpha = 1.0f;
         a.beta = 0.0f;
@@ -421,7 +432,8 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
     // (16-bit C always goes through the row-store epilogue.)
     const bool c_tma = split ? p->ws_tma
-                             : p->c_half == 0 && p->N % 4 == 0 && ldc % 4 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0;
+                             : p->c_half == 0 && p->N % 4 == 0 && ldc % 4 == 0 &&
+                                   reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
     if (use_tma && p->sk_tiles > 0) {
@@ -602,7 +614,8 @@ int gemm_plan_status(const gemm_plan* p)
     if (h) {
         // A launch that gave up may have left stream-K counters short of its
         // number: start the numbering again from cleared counters.
-        if (p->sk_flags && cudaMemset(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned)) == cudaSuccess)
+        const size_t bytes = static_cast<size_t>(p->sk_ctas) * sizeof(unsigned);
+        if (p->sk_flags && cudaMemset(p->sk_flags, 0, bytes) == cudaSuccess)
             p->sk_epoch.store(0);
         return fail(GEMM_ERR_TIMEOUT, "a bounded wait gave up inside the kernel (error bits 0x%x)", h);
     }

@@ -14,7 +14,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 
@@ -52,17 +51,6 @@ __global__ void __launch_bounds__(ProbeTraits<DT>::THREADS, 1)
     }
 }
 
-int fail(int code, const char* fmt, ...)
-{
-    char msg[512];
-    va_list ap;
-    va_start(ap, fmt);
-    std::vsnprintf(msg, sizeof msg, fmt, ap);
-    va_end(ap);
-    sat::set_last_error(msg);
-    return code;
-}
-
 template <int DT>
 cudaError_t launch_probe(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC, const GemmArgs* a,
                          int grid, cudaStream_t stream)
@@ -85,23 +73,24 @@ extern "C" int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_d
     const int dt = static_cast<int>(dtype);
     if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) ||
         dt < 0 || dt > 2)
-        return fail(GEMM_ERR_ARG, "bad dimensions or dtype");
+        return sat::fail_with(GEMM_ERR_ARG, "bad dimensions or dtype");
     if (!A || !B || !C)
-        return fail(GEMM_ERR_ARG, "NULL operand");
+        return sat::fail_with(GEMM_ERR_ARG, "NULL operand");
     const int es = dt == 0 ? 4 : 2;
     if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16 ||
         reinterpret_cast<uintptr_t>(C) % 16 || (K * es) % 16 || (N * es) % 16 || N % 4)
-        return fail(GEMM_ERR_ALIGN, "the device-call self-test takes 16-byte aligned operands and row strides");
+        return sat::fail_with(GEMM_ERR_ALIGN,
+                              "the device-call self-test takes 16-byte aligned operands and row strides");
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "querying the device: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "querying the device: %s", cudaGetErrorString(e));
 
     const sat::KernelEntry* k = sat::find_entry(dt, 128, 1, sat::kProdTMA);
     if (!k)
-        return fail(GEMM_ERR_ARG, "no 128 x 128 kernel for this dtype");
+        return sat::fail_with(GEMM_ERR_ARG, "no 128 x 128 kernel for this dtype");
     GemmArgs a{};
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -109,9 +98,9 @@ extern "C" int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_d
     a.A = A;
     a.B = B;
     a.C = C;
-    a.lda = K;
-    a.ldb = N;
-    a.ldc = N;
+    a.lda = static_cast<int>(K);
+    a.ldb = static_cast<int>(N);
+    a.ldc = static_cast<int>(N);
     a.alpha = alpha;
     a.beta = beta;
     a.tiles_m = static_cast<int>((M + 127) / 128);
@@ -134,13 +123,13 @@ extern "C" int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_d
         sat::encode_map(&tmB, tdt, es, B, N, K, N, static_cast<uint32_t>(128 / es), static_cast<uint32_t>(k->bk),
                         static_cast<CUtensorMapSwizzle>(k->b_swizzle)) ||
         sat::encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, N, 32u, 32u, CU_TENSOR_MAP_SWIZZLE_128B))
-        return fail(GEMM_ERR_LAUNCH, "encoding the tensor maps");
+        return sat::fail_with(GEMM_ERR_LAUNCH, "encoding the tensor maps");
     const int grid = static_cast<int>(a.num_tiles < sms ? a.num_tiles : sms);
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     e = dt == 0   ? launch_probe<0>(&tmA, &tmB, &tmC, &a, grid, stream)
         : dt == 1 ? launch_probe<1>(&tmA, &tmB, &tmC, &a, grid, stream)
                   : launch_probe<2>(&tmA, &tmB, &tmC, &a, grid, stream);
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "launching the megakernel: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "launching the megakernel: %s", cudaGetErrorString(e));
     return GEMM_OK;
 }

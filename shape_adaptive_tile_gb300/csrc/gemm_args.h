@@ -23,8 +23,8 @@ struct GemmArgs {
     const void* A;             // M x K row-major (plain-load producer only)
     const void* B;             // K x N row-major (plain-load producer only)
     float* C;                  // output: C (M x N), or the split-K workspace (splits x out_rows x N)
-    int64_t lda, ldb;          // row strides of A and B in elements (plain-load producer only)
-    int64_t ldc;               // row stride of the output the kernel writes, in elements
+    int lda, ldb;              // row strides of A and B in elements (plain-load producer only); < 2^31
+    int ldc;                   // row stride of the output the kernel writes, in elements; < 2^31
     int c_half;                // element type of C: 0 fp32, 1 bf16, 2 fp16 (16-bit C: row-store epilogue only)
     float alpha, beta;
     int tiles_m, tiles_n;      // tiles of (128 * cta_group) x BN

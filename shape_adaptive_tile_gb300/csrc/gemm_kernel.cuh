@@ -97,24 +97,23 @@ struct Traits {
     static constexpr bool C_RING_OK = PROD == kProdTMA && NCS + 2 <= STAGES;
     static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
     static constexpr uint32_t FMT = DT == kDtTF32 ? kFmtTF32 : DT == kDtBF16 ? kFmtBF16 : kFmtF16;
-    // B in shared memory. TMA copies B as it lies in memory (N contiguous,
-    // "MN-major"); 16-bit types use the 128-byte swizzle, 32-bit (tf32)
-    // types the 128-byte swizzle with 32-byte atoms, the only MN-major
-    // swizzle the tensor core takes for 32-bit operands. The plain-load
-    // producer of tf32 instead stores B transposed, K-major like A.
-    static constexpr bool B_MN = true;
-    static constexpr uint32_t B_LAYOUT = kTF32 ? kLayoutSW128Atom32 : kLayoutSW128;
+    // Operand tiles in shared memory, each as it lies in memory.
+    // MN-major (M or N contiguous): 16-bit types in the 128-byte swizzle,
+    // 32-bit (tf32) types in the 128-byte swizzle with 32-byte atoms, the only
+    // MN-major swizzle the tensor core takes for 32-bit operands; 128-byte
+    // column blocks are BK*128 bytes apart (leading byte offset); K rows come
+    // in swizzle groups, 8 rows (1024 bytes) for 16-byte atoms and 4 rows (512
+    // bytes) for 32-byte atoms (stride byte offset); one MMA step of K advances
+    // UK rows of 128 bytes. K-major: rows of 128 bytes in the 128-byte swizzle,
+    // 8-row groups 1024 bytes apart; one MMA step of K advances 32 bytes
+    // inside the swizzled row. The plain-load producers write the same
+    // layouts (B MN-major) themselves.
     static constexpr uint32_t IDESC = idesc_f32acc(FMT, BM * CG, BN, !B_KM, A_MN);
-    // MN-major: 128-byte column blocks are BK*128 bytes apart (leading byte
-    // offset); K rows come in swizzle groups, 8 rows (1024 bytes) for the
-    // 16-byte-atom swizzle and 4 rows (512 bytes) for the 32-byte-atom one
-    // (stride byte offset); one MMA step of K advances UK rows of 128 bytes.
-    // K-major: rows of 128 bytes, 8-row groups 1024 bytes apart, and one step
-    // of K advances 32 bytes inside the swizzled row.
-    static constexpr uint32_t B_LBO = B_MN ? BK * 128 : 16;
-    static constexpr uint32_t B_SBO = B_LAYOUT == kLayoutSW128Atom32 ? 512 : 1024;
-    static constexpr uint32_t B_KSTEP = B_MN ? UK * 128 : UK * ES;
-    static constexpr uint32_t A_KSTEP = UK * ES;    // bytes per MMA step of K in A (= 32)
+    static constexpr uint32_t MN_LAYOUT = kTF32 ? kLayoutSW128Atom32 : kLayoutSW128;
+    static constexpr uint32_t MN_LBO = BK * 128;
+    static constexpr uint32_t MN_SBO = MN_LAYOUT == kLayoutSW128Atom32 ? 512 : 1024;
+    static constexpr uint32_t MN_KSTEP = UK * 128;
+    static constexpr uint32_t K_KSTEP = UK * ES;     // = 32
 
     static_assert(B_KM || BN % (CW * CG) == 0, "B tile must be whole swizzle rows per CTA");
     static_assert(!B_KM || BN_CTA % 8 == 0, "K-major tile: whole 8-row swizzle groups");
@@ -350,6 +349,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
 
     if (warp < T::NPW) {
         // ------------------------------------------------------------ producer
+
         if constexpr (T::TMA) {
             if (lane == 0) {
                 int stage = 0;
@@ -635,7 +635,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
             WorkIter it = work_begin(args, tile0);
             Unit w;
             while (ok && work_next(args, tile_step, it, w)) {
-                if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {  // peer epilogue releases: cluster scope
+                // The peer's epilogue releases the accumulator too: cluster scope.
+                if (!wait_bar<kClu>(tempty_bar(acc), acc_phase ^ 1u, wc, kErrTimeoutMma)) {
                     ok = false;
                     break;
                 }
@@ -655,10 +656,10 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                         // K-major operands: 128-byte rows, one MMA step of K
                         // 32 bytes on; MN-major: column blocks BK*128 bytes
                         // apart, one MMA step of K UK rows on.
-                        const uint64_t ad = T::A_MN ? sdesc(a0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT)
-                                                    : sdesc(a0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128);
-                        const uint64_t bd = T::B_KM ? sdesc(b0 + ks * T::A_KSTEP, 16, 1024, kLayoutSW128)
-                                                    : sdesc(b0 + ks * T::B_KSTEP, T::B_LBO, T::B_SBO, T::B_LAYOUT);
+                        const uint64_t ad = T::A_MN ? sdesc(a0 + ks * T::MN_KSTEP, T::MN_LBO, T::MN_SBO, T::MN_LAYOUT)
+                                                    : sdesc(a0 + ks * T::K_KSTEP, 16, 1024, kLayoutSW128);
+                        const uint64_t bd = T::B_KM ? sdesc(b0 + ks * T::K_KSTEP, 16, 1024, kLayoutSW128)
+                                                    : sdesc(b0 + ks * T::MN_KSTEP, T::MN_LBO, T::MN_SBO, T::MN_LAYOUT);
                         mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb != w.kb0 || ks != 0) ? 1u : 0u);
                     }
                     issued = true;
@@ -713,7 +714,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
         int acc = 0;
         uint32_t acc_phase = 0;
         const float alpha = args.alpha, beta = args.beta;
-        const int64_t ldc = args.ldc;
+        const int ldc = args.ldc;
         constexpr int NCHUNK = BN / 32;
         // C values (bulk-store path, beta != 0) of row (row0 + lane), columns
         // gcol0 .. gcol0 + 31, as 8 aligned float4 loads; zero outside M x N.
@@ -828,7 +829,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                         if (w.kind != kWhole) {
                             const int row = sub * 32 + lane;
                             if (w.kind == kSkPartial) {
-                                float* slot = args.sk_ws + static_cast<int64_t>(tile0 * CG + static_cast<int>(rank)) * (128 * BN);
+                                float* slot =
+                                    args.sk_ws + static_cast<int64_t>(tile0 * CG + static_cast<int>(rank)) * (128 * BN);
 #pragma unroll
                                 for (int q = 0; q < 8; ++q)
                                     st_global_v4(slot + ((c * 8 + q) * 128 + row) * 4, __uint_as_float(r[4 * q]),
@@ -896,7 +898,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                                     float v = alpha * __uint_as_float(r[j]);
                                     if (beta != 0.0f)
                                         v = fmaf(beta, ct[j], v);
-                                    c_store(args.C, args.c_half, c0 + j * ldc, v);
+                                    c_store(args.C, args.c_half, c0 + static_cast<int64_t>(j) * ldc, v);
                                 }
                             }
                         }
@@ -986,8 +988,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                         for (int i = 0; i < rows; ++i) {
                             float v = alpha * buf[i * 32 + (lane ^ i)];
                             if (beta != 0.0f)
-                                v = fmaf(beta, c_load(args.C, kind, c0 + i * ldc), v);
-                            c_store(args.C, kind, c0 + i * ldc, v);
+                                v = fmaf(beta, c_load(args.C, kind, c0 + static_cast<int64_t>(i) * ldc), v);
+                            c_store(args.C, kind, c0 + static_cast<int64_t>(i) * ldc, v);
                         }
                     }
                     __syncwarp();

@@ -77,7 +77,7 @@ constexpr KernelEntry make_entry()
                        T::THREADS,
                        T::SMEM_BYTES,
                        T::BK,
-                       T::B_LAYOUT == kLayoutSW128Atom32 ? static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)
+                       T::MN_LAYOUT == kLayoutSW128Atom32 ? static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)
                                                          : static_cast<int>(CU_TENSOR_MAP_SWIZZLE_128B),
                        T::C_RING_OK ? 1 : 0,
                        T::A_MN ? 1 : 0,

@@ -15,7 +15,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -45,18 +44,6 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// Failures are reported through gemm_last_error(), like every other entry point.
-int fail(int code, const char* fmt, ...)
-{
-    char msg[512];
-    va_list ap;
-    va_start(ap, fmt);
-    std::vsnprintf(msg, sizeof msg, fmt, ap);
-    va_end(ap);
-    sat::set_last_error(msg);
-    return code;
-}
-
 // Row-major 2-D tensor map, 128-byte-swizzled boxes, zero fill outside.
 bool encode(CUtensorMap* map, CUtensorMapDataType t, int es, const void* ptr, uint64_t inner, uint64_t outer,
             uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
@@ -69,7 +56,8 @@ bool encode(CUtensorMap* map, CUtensorMapDataType t, int es, const void* ptr, ui
 int setup_device(int dev, DeviceState** out)
 {
     if (dev < 0 || dev >= kMaxDevices)
-        return fail(GEMM_ERR_ARG, "device %d is beyond the %d devices this entry point tracks", dev, kMaxDevices);
+        return sat::fail_with(GEMM_ERR_ARG, "device %d is beyond the %d devices this entry point tracks", dev,
+                              kMaxDevices);
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& s = g_dev[dev];
     if (!s.ready) {
@@ -80,14 +68,15 @@ int setup_device(int dev, DeviceState** out)
         if (e == cudaSuccess)
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
-            return fail(GEMM_ERR_LAUNCH, "querying device %d: %s", dev, cudaGetErrorString(e));
+            return sat::fail_with(GEMM_ERR_LAUNCH, "querying device %d: %s", dev, cudaGetErrorString(e));
         if (major != 10 || minor != 3)
-            return fail(GEMM_ERR_ARCH, "device %d is compute capability %d.%d; this library is built for sm_103a only",
+            return sat::fail_with(GEMM_ERR_ARCH,
+                                  "device %d is compute capability %d.%d; this library is built for sm_103a only",
                         dev, major, minor);
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || !ptr)
-            return fail(GEMM_ERR_LAUNCH, "cudaGetSymbolAddress of the scratch array on device %d: %s", dev,
+            return sat::fail_with(GEMM_ERR_LAUNCH, "cudaGetSymbolAddress of the scratch array on device %d: %s", dev,
                         cudaGetErrorString(e));
         s.scratch = ptr;
         s.sm_count = sms;
@@ -126,19 +115,19 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     sat::set_last_error("");
     const int dt = static_cast<int>(dtype);
     if (M < 0 || N < 0 || K < 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
-        return fail(GEMM_ERR_ARG, "dimensions must be in [0, 2^31)");
+        return sat::fail_with(GEMM_ERR_ARG, "dimensions must be in [0, 2^31)");
     if (dt < 0 || dt > 2)
-        return fail(GEMM_ERR_ARG, "unknown dtype %d", dt);
+        return sat::fail_with(GEMM_ERR_ARG, "unknown dtype %d", dt);
     if (M == 0 || N == 0)
         return GEMM_OK;
     if (!C)
-        return fail(GEMM_ERR_ARG, "C is NULL");
+        return sat::fail_with(GEMM_ERR_ARG, "C is NULL");
     if (reinterpret_cast<uintptr_t>(C) % 4 != 0)
-        return fail(GEMM_ERR_ALIGN, "C must be 4-byte aligned");
+        return sat::fail_with(GEMM_ERR_ALIGN, "C must be 4-byte aligned");
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "cudaGetDevice: %s", cudaGetErrorString(e));
     DeviceState* ds = nullptr;
     int rc = setup_device(dev, &ds);
     if (rc)
@@ -146,13 +135,14 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (K == 0 || alpha == 0.0f) {
         e = sat::launch_scale(C, 0, M, N, N, beta, stream);
-        return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_LAUNCH, "beta-scale kernel: %s", cudaGetErrorString(e));
+        return e == cudaSuccess ? GEMM_OK
+                                : sat::fail_with(GEMM_ERR_LAUNCH, "beta-scale kernel: %s", cudaGetErrorString(e));
     }
     if (!A || !B)
-        return fail(GEMM_ERR_ARG, "A or B is NULL");
+        return sat::fail_with(GEMM_ERR_ARG, "A or B is NULL");
     const int es = dt == 0 ? 4 : 2;
     if (reinterpret_cast<uintptr_t>(A) % es || reinterpret_cast<uintptr_t>(B) % es)
-        return fail(GEMM_ERR_ALIGN, "A and B must be aligned to their %d-byte element size", es);
+        return sat::fail_with(GEMM_ERR_ALIGN, "A and B must be aligned to their %d-byte element size", es);
 
     // The same choice gemm_plan_create would make.
     const bool tma_ok = (K * es) % 16 == 0 && (N * es) % 16 == 0;
@@ -161,7 +151,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     const sat::KernelEntry* k = use_tma ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA)
                                         : sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
     if (!k)
-        return fail(GEMM_ERR_ARG, "no compiled kernel for the chosen configuration");
+        return sat::fail_with(GEMM_ERR_ARG, "no compiled kernel for the chosen configuration");
     const int64_t num_kb = (K + k->bk - 1) / k->bk;
     int splits = c.splits > 1 && num_kb > 1 ? c.splits : 1;
     if (splits > num_kb)
@@ -173,7 +163,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     const int64_t ws_rows = (M + tile_rows - 1) / tile_rows * tile_rows;
     const size_t ws_bytes = splits > 1 ? static_cast<size_t>(splits) * ws_rows * static_cast<size_t>(N) * 4 : 0;
     if (ws_bytes > kWorkspaceBytes)
-        return fail(GEMM_ERR_ARG,
+        return sat::fail_with(GEMM_ERR_ARG,
                     "this problem splits K %d ways and needs %zu bytes of scratch; the allocation-free entry point "
                     "has %zu bytes (use gemm_plan_create/gemm_run, which allocate their own workspace)",
                     splits, ws_bytes, kWorkspaceBytes);
@@ -189,7 +179,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
             sk_ctas = slots * k->cg;
             const size_t need = static_cast<size_t>(sk_ctas) * 128 * k->bn * 4;
             if (need > kWorkspaceBytes || kCounterOffset + static_cast<size_t>(sk_ctas) * 4 > kStatusBytes)
-                return fail(GEMM_ERR_ARG,
+                return sat::fail_with(GEMM_ERR_ARG,
                             "this problem's stream-K partial tiles need %zu bytes of scratch; the allocation-free "
                             "entry point has %zu bytes (use gemm_plan_create/gemm_run)",
                             need, kWorkspaceBytes);
@@ -197,7 +187,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     }
     e = k->prepare();
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "setting the kernel's shared-memory limit: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "setting the kernel's shared-memory limit: %s", cudaGetErrorString(e));
 
     uint32_t* status = static_cast<uint32_t*>(ds->scratch);
     float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(ds->scratch) + kStatusBytes);
@@ -205,7 +195,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     // stream-K counters must start at zero (this call is launch number 1).
     e = cudaMemsetAsync(status, 0, kStatusBytes, stream);
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
 
     sat::GemmArgs a{};
     a.M = static_cast<int>(M);
@@ -213,9 +203,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     a.K = static_cast<int>(K);
     a.A = A;
     a.B = B;
-    a.lda = K;
-    a.ldb = N;
-    a.ldc = N;
+    a.lda = static_cast<int>(K);
+    a.ldb = static_cast<int>(N);
+    a.ldc = static_cast<int>(N);
     a.C = splits > 1 ? ws : C;
     a.alpha = splits > 1 ? 1.0f : alpha;
     a.beta = splits > 1 ? 0.0f : beta;
@@ -241,7 +231,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     if (c_tma && !encode(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.C, N,
                          splits > 1 ? static_cast<uint64_t>(splits) * ws_rows : static_cast<uint64_t>(M), 32u, 32u,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-        return fail(GEMM_ERR_LAUNCH, "encoding the output tensor map");
+        return sat::fail_with(GEMM_ERR_LAUNCH, "encoding the output tensor map");
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = !c.cload && use_tma && k->c_ring && c_tma && splits == 1 && sk_tiles == 0 && beta != 0.0f ? 1 : 0;
     if (sk_tiles > 0) {
@@ -256,17 +246,17 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
                     k->prod == sat::kProdSwap ? static_cast<uint32_t>(k->bn) : 128u, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode(&tmB, tdt, es, B, N, K, static_cast<uint32_t>(128 / es), static_cast<uint32_t>(k->bk),
                     static_cast<CUtensorMapSwizzle>(k->b_swizzle)))
-            return fail(GEMM_ERR_LAUNCH, "encoding the operand tensor maps");
+            return sat::fail_with(GEMM_ERR_LAUNCH, "encoding the operand tensor maps");
     }
-    e = k->launch(&tmA, &tmB, &tmC, &a, sk_tiles > 0 ? static_cast<int>(sk_ctas) : grid_for(M, N, splits, ds->sm_count, k),
-                  stream);
+    const int grid = sk_tiles > 0 ? static_cast<int>(sk_ctas) : grid_for(M, N, splits, ds->sm_count, k);
+    e = k->launch(&tmA, &tmB, &tmC, &a, grid, stream);
     if (e != cudaSuccess)
-        return fail(GEMM_ERR_LAUNCH, "launching the GEMM kernel: %s", cudaGetErrorString(e));
+        return sat::fail_with(GEMM_ERR_LAUNCH, "launching the GEMM kernel: %s", cudaGetErrorString(e));
     if (splits > 1) {
         e = sat::launch_splitk_reduce(ws, splits, static_cast<long long>(ws_rows) * N, C, 0, M, N, N, alpha, beta,
                                       ds->sm_count, stream);
         if (e != cudaSuccess)
-            return fail(GEMM_ERR_LAUNCH, "launching the split-K reduction: %s", cudaGetErrorString(e));
+            return sat::fail_with(GEMM_ERR_LAUNCH, "launching the split-K reduction: %s", cudaGetErrorString(e));
     }
     return GEMM_OK;
 }

@@ -18,7 +18,7 @@ struct KernelEntry {
     int threads;   // CTA size
     int smem;      // dynamic shared memory bytes
     int bk;        // K per stage
-    int b_swizzle; // CUtensorMapSwizzle of B's tensor map
+    int b_swizzle; // CUtensorMapSwizzle of MN-major operand boxes (B as it lies, or A stored K x M)
     int c_ring;    // 1: with beta != 0 the producer can fetch C through the operand ring
     int a_mn;      // 1: the first MMA operand is read MN-major (A stored K x M, or B for a swapped tile)
     int b_km;      // 1: the second MMA operand is read K-major (B stored N x K, or A for a swapped tile)
@@ -38,6 +38,9 @@ extern const int kNumEntriesFP16;
 
 // Sets the message gemm_last_error() returns on this thread (api.cu).
 void set_last_error(const char* msg);
+
+// Sets that message from a printf format and returns `code` (api.cu).
+int fail_with(int code, const char* fmt, ...);
 
 // Encodes a 2-D tensor map of a row-major matrix: `outer` rows of `inner`
 // elements, `ld` elements apart, read or written in boxes of box_inner x

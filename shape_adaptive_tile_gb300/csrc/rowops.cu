@@ -16,7 +16,6 @@
 
 #include <cuda_runtime.h>
 
-#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 
@@ -174,17 +173,6 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-int fail(int code, const char* fmt, ...)
-{
-    char msg[512];
-    va_list ap;
-    va_start(ap, fmt);
-    std::vsnprintf(msg, sizeof msg, fmt, ap);
-    va_end(ap);
-    sat::set_last_error(msg);
-    return code;
-}
-
 template <int OP, int PER, int VEC>
 cudaError_t launch_one(const float* X, int64_t ldx, const float* gamma, const float* beta, float* Y, int64_t ldy,
                        int64_t rows, int width, float eps, cudaStream_t stream)
@@ -217,19 +205,20 @@ int run(const float* X, int64_t ldx, const float* gamma, const float* beta, floa
 {
     sat::set_last_error("");
     if (rows < 0 || width < 0)
-        return fail(GEMM_ERR_ARG, "negative size");
+        return sat::fail_with(GEMM_ERR_ARG, "negative size");
     if (rows == 0 || width == 0)
         return GEMM_OK;
     if (width > kRowopMaxWidth)
-        return fail(GEMM_ERR_ARG, "width %lld is above the %d these kernels hold in registers", (long long)width,
+        return sat::fail_with(GEMM_ERR_ARG, "width %lld is above the %d these kernels hold in registers",
+                              (long long)width,
                     kRowopMaxWidth);
     if (!X || !Y)
-        return fail(GEMM_ERR_ARG, "X or Y is NULL");
+        return sat::fail_with(GEMM_ERR_ARG, "X or Y is NULL");
     if (ldx < width || ldy < width)
-        return fail(GEMM_ERR_ARG, "row stride below the width");
+        return sat::fail_with(GEMM_ERR_ARG, "row stride below the width");
     if (reinterpret_cast<uintptr_t>(X) % 4 || reinterpret_cast<uintptr_t>(Y) % 4 ||
         (gamma && reinterpret_cast<uintptr_t>(gamma) % 4) || (beta && reinterpret_cast<uintptr_t>(beta) % 4))
-        return fail(GEMM_ERR_ALIGN, "operands must be 4-byte aligned");
+        return sat::fail_with(GEMM_ERR_ALIGN, "operands must be 4-byte aligned");
     auto al16 = [](const void* p) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % 16 == 0; };
     const bool vec = width % 4 == 0 && ldx % 4 == 0 && ldy % 4 == 0 && al16(X) && al16(Y) && al16(gamma) &&
                      al16(beta);
@@ -237,7 +226,8 @@ int run(const float* X, int64_t ldx, const float* gamma, const float* beta, floa
     const int w = static_cast<int>(width);
     const cudaError_t e = vec ? launch_vec<OP, 4>(X, ldx, gamma, beta, Y, ldy, rows, w, eps, s)
                               : launch_vec<OP, 1>(X, ldx, gamma, beta, Y, ldy, rows, w, eps, s);
-    return e == cudaSuccess ? GEMM_OK : fail(GEMM_ERR_LAUNCH, "launching the row kernel: %s", cudaGetErrorString(e));
+    return e == cudaSuccess ? GEMM_OK
+                            : sat::fail_with(GEMM_ERR_LAUNCH, "launching the row kernel: %s", cudaGetErrorString(e));
 }
 
 }  // namespace
