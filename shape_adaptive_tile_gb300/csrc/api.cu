@@ -87,6 +87,7 @@ struct gemm_plan {
     bool c_ring = false;  // beta != 0: the producer fetches C through the operand ring
     const sat::KernelEntry* tma = nullptr;    // null when the strides rule out TMA
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
+    const sat::KernelEntry* plain_strided = nullptr;  // the same, for row strides other than K and N
     int grid_tma = 0, grid_plain = 0;
     uint32_t* d_err = nullptr;
     // Split-K: `splits` slices of `ws_rows` x N floats in `ws`, reduced in
@@ -253,13 +254,14 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
     }
     if (!trans) {
         p->plain = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
-        if (!p->plain) {
+        p->plain_strided = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlainStrided);
+        if (!p->plain || !p->plain_strided) {
             fail(GEMM_ERR_ARG, "no compiled plain-load kernel for bn=%d", c.bn);
             delete p;
             return nullptr;
         }
     }
-    for (const sat::KernelEntry* k : {p->tma, p->plain}) {
+    for (const sat::KernelEntry* k : {p->tma, p->plain, p->plain_strided}) {
         if (!k)
             continue;
         e = k->prepare();
@@ -388,7 +390,8 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         return fail(GEMM_ERR_ALIGN,
                     "transposed operands are read by TMA only: A and B must be 16-byte aligned with row strides "
                     "that are multiples of 16 bytes");
-    const sat::KernelEntry* k = use_tma ? p->tma : p->plain;
+    const bool dense = lda == p->K && ldb == p->N;
+    const sat::KernelEntry* k = use_tma ? p->tma : dense ? p->plain : p->plain_strided;
 
     sat::GemmArgs a{};
     a.M = static_cast<int>(p->M);

@@ -17,6 +17,7 @@ constexpr int kProdSwap = 2;   // TMA loads, operand roles exchanged: the MMA co
 constexpr int kProdTN = 3;     // TMA loads, A stored transposed (K x M): first operand MN-major
 constexpr int kProdNT = 4;     // TMA loads, B stored transposed (N x K): second operand K-major
 constexpr int kProdTT = 5;     // TMA loads, both stored transposed
+constexpr int kProdPlainStrided = 6;  // plain loads with row strides lda, ldb other than K, N
 
 struct GemmArgs {
     int M, N, K;

@@ -91,6 +91,7 @@ constexpr KernelEntry make_entry()
     make_entry<DT, 64, 1, kProdTMA>(), make_entry<DT, 128, 1, kProdTMA>(), make_entry<DT, 256, 1, kProdTMA>(), \
         make_entry<DT, 128, 2, kProdTMA>(), make_entry<DT, 256, 2, kProdTMA>(),                                 \
         make_entry<DT, 128, 1, kProdPlain>(), make_entry<DT, 256, 1, kProdPlain>(),                             \
+        make_entry<DT, 128, 1, kProdPlainStrided>(), make_entry<DT, 256, 1, kProdPlainStrided>(),               \
         make_entry<DT, 32, 1, kProdSwap>(), make_entry<DT, 64, 1, kProdSwap>(), make_entry<DT, 128, 1, kProdSwap>(), \
         make_entry<DT, 128, 1, kProdTN>(), make_entry<DT, 256, 1, kProdTN>(), make_entry<DT, 256, 2, kProdTN>(),    \
         make_entry<DT, 128, 1, kProdNT>(), make_entry<DT, 256, 1, kProdNT>(), make_entry<DT, 256, 2, kProdNT>(),    \

@@ -13,7 +13,7 @@ struct KernelEntry {
     int dt;        // kDtTF32 / kDtBF16 / kDtFP16
     int bn;        // N of the output tile
     int cg;        // 1: one SM per 128-row tile; 2: a CTA pair (cluster of 2) per 256-row tile
-    int prod;      // kProdTMA / kProdPlain / kProdSwap
+    int prod;      // kProdTMA, kProdPlain, kProdSwap, kProdTN/NT/TT or kProdPlainStrided
     int stages;    // shared-memory ring depth
     int threads;   // CTA size
     int smem;      // dynamic shared memory bytes
