@@ -4,14 +4,14 @@
 // These are the wide-row reductions of "Scale coverage exposes a remaining
 // GEMM gap" (section "Reductions: wide rows and large working sets"),
 // 37 x 8191 to 16384 x 4096. They read each element once and write it once,
-// so HBM bandwidth bounds them: 8 bytes per element. One CTA of 512 threads
-// takes a row; each thread keeps its PER elements of the row in registers
-// between the reductions and the write, so the row is read from memory once.
-// Loads are 16 bytes wide where the row start, the row strides and the width
-// allow it, 4 bytes otherwise; consecutive threads read consecutive
-// addresses either way. Reductions go warp by warp with shuffles, then
-// across the 16 warps through shared memory, in a fixed order: the result
-// is the same on every run.
+// so HBM bandwidth bounds them: 8 bytes per element. One CTA of 128 to 512
+// threads takes a row; each thread keeps its PER elements of the row in
+// registers between the reductions and the write, so the row is read from
+// memory once. Loads are 16 bytes wide where the row start, the row strides
+// and the width allow it, 4 bytes otherwise; consecutive threads read
+// consecutive addresses either way. Reductions go warp by warp with
+// shuffles, then across the CTA's warps through shared memory, in a fixed
+// order: the result is the same on every run.
 #include "rowops.h"
 
 #include <cuda_runtime.h>
@@ -23,17 +23,20 @@
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 
 enum Op { kSoftmax = 0, kRMSNorm = 1, kLayerNorm = 2 };
+
+// exp(d) is computed as 2^(d log2 e): exp2f is cheaper than expf, and the
+// rounding of d log2 e adds a relative error of about |d| 2^-24 ln 2, below
+// 1e-6 for the |d| < 16 of rows of order one. d = 0 still gives exactly 1.
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Sum (or maximum) over the block, the same value returned to every thread.
 // Consecutive reductions alternate between two scratch rows, so one barrier
 // each suffices: a row is rewritten only two reductions later, after a
 // barrier that every thread passed after reading it.
-template <bool kMax>
-__device__ __forceinline__ float block_reduce(float v, float (*scratch)[kWarps], int& turn)
+template <bool kMax, int NW>
+__device__ __forceinline__ float block_reduce(float v, float (*scratch)[NW], int& turn)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -46,7 +49,7 @@ __device__ __forceinline__ float block_reduce(float v, float (*scratch)[kWarps],
     if (lane == 0)
         row[warp] = v;
     __syncthreads();
-    float t = lane < kWarps ? row[lane] : (kMax ? -INFINITY : 0.0f);
+    float t = lane < NW ? row[lane] : (kMax ? -INFINITY : 0.0f);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float u = __shfl_xor_sync(0xffffffffu, t, o);
@@ -55,23 +58,24 @@ __device__ __forceinline__ float block_reduce(float v, float (*scratch)[kWarps],
     return t;
 }
 
-// Element e of this thread's share: column e * kThreads * VEC + threadIdx.x * VEC
-// + (lane within the vector). VEC = 4 loads 16 bytes at a time.
-template <int OP, int PER, int VEC>
-__global__ void __launch_bounds__(kThreads)
+// NT threads (one CTA) take a row; element e of a thread's share is column
+// e / VEC * NT * VEC + threadIdx.x * VEC + e % VEC. VEC = 4 loads 16 bytes
+// at a time.
+template <int OP, int NT, int PER, int VEC>
+__global__ void __launch_bounds__(NT)
     sat_rowop_kernel(const float* X, int64_t ldx, const float* __restrict__ gamma,
                      const float* __restrict__ beta, float* Y, int64_t ldy, int64_t rows, int width,
                      float eps)
 {
-    __shared__ float scratch[2][kWarps];
+    constexpr int NW = NT / 32;  // warps per row
+    __shared__ float scratch[2][NW];
     int turn = 0;
     constexpr int NV = PER / VEC;  // vectors per thread
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    auto load_row = [&](float(&v)[PER], int64_t r) {
         const float* x = X + r * ldx;
-        float v[PER];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            const int c = (i * kThreads + threadIdx.x) * VEC;
+            const int c = (i * NT + threadIdx.x) * VEC;
             if constexpr (VEC == 4) {
                 float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (c < width)
@@ -84,7 +88,11 @@ __global__ void __launch_bounds__(kThreads)
                 v[i] = c < width ? x[c] : 0.0f;
             }
         }
-        auto valid = [&](int i) { return (i / VEC * kThreads + threadIdx.x) * VEC + i % VEC < width; };
+    };
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        float v[PER];
+        load_row(v, r);
+        auto valid = [&](int i) { return (i / VEC * NT + threadIdx.x) * VEC + i % VEC < width; };
         float scale = 0.0f, shift = 0.0f;
         if constexpr (OP == kSoftmax) {
             float m = -INFINITY;
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(kThreads)
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
-                v[i] = valid(i) ? expf(v[i] - m) : 0.0f;
+                v[i] = valid(i) ? exp2f((v[i] - m) * kLog2e) : 0.0f;
                 s += v[i];
             }
             s = block_reduce<false>(s, scratch, turn);
@@ -126,7 +134,7 @@ __global__ void __launch_bounds__(kThreads)
         float* y = Y + r * ldy;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            const int c = (i * kThreads + threadIdx.x) * VEC;
+            const int c = (i * NT + threadIdx.x) * VEC;
             if (c >= width)
                 continue;
             // gamma and beta for these VEC columns, 16 bytes at a time when VEC is 4
@@ -173,13 +181,13 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int OP, int PER, int VEC>
+template <int OP, int NT, int PER, int VEC>
 cudaError_t launch_one(const float* X, int64_t ldx, const float* gamma, const float* beta, float* Y, int64_t ldy,
                        int64_t rows, int width, float eps, cudaStream_t stream)
 {
     const int64_t grid = rows < 65535 ? rows : 65535;
-    sat_rowop_kernel<OP, PER, VEC><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(X, ldx, gamma, beta, Y, ldy,
-                                                                                        rows, width, eps);
+    sat_rowop_kernel<OP, NT, PER, VEC><<<static_cast<unsigned>(grid), NT, 0, stream>>>(X, ldx, gamma, beta, Y, ldy,
+                                                                                       rows, width, eps);
     return cudaGetLastError();
 }
 
@@ -187,16 +195,33 @@ template <int OP, int VEC>
 cudaError_t launch_vec(const float* X, int64_t ldx, const float* g, const float* b, float* Y, int64_t ldy,
                        int64_t rows, int width, float eps, cudaStream_t s)
 {
-    // The smallest register share that holds the row.
-    if (width <= kThreads * 4)
-        return launch_one<OP, 4, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-    if (width <= kThreads * 8)
-        return launch_one<OP, 8, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-    if (width <= kThreads * 16)
-        return launch_one<OP, 16, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-    if (width <= kThreads * 32)
-        return launch_one<OP, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-    return launch_one<OP, 64, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    // Rows of 16-byte vectors from 2049 to 8192 columns: fewer threads per
+    // row, each holding more of it. That spreads the per-row work (the
+    // reductions, the scale, the index arithmetic) over more elements and
+    // keeps more loads in flight per thread; the thread counts are the
+    // fastest measured per operator on GB300 (rows x 4096 and x 8192).
+    if constexpr (VEC == 4) {
+        if (width > 2048 && width <= 4096) {
+            if constexpr (OP == kLayerNorm)
+                return launch_one<OP, 128, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+            else
+                return launch_one<OP, 256, 16, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+        }
+        if constexpr (OP != kRMSNorm) {
+            if (width > 4096 && width <= 8192)
+                return launch_one<OP, 256, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+        }
+    }
+    // Otherwise 512 threads, with the smallest register share that holds the row.
+    if (width <= 512 * 4)
+        return launch_one<OP, 512, 4, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= 512 * 8)
+        return launch_one<OP, 512, 8, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= 512 * 16)
+        return launch_one<OP, 512, 16, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    if (width <= 512 * 32)
+        return launch_one<OP, 512, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+    return launch_one<OP, 512, 64, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
 }
 
 template <int OP>
