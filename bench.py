@@ -217,13 +217,13 @@ def job_value(flops_per_step, steps, job_ms, world):
 
 def traffic_for(desc):
     """DRAM bytes per launch recorded from an ncu capture of this exact
-    kernel source, or None (no capture, or the source changed since)."""
-    from shape_adaptive_tile_gb300.build import source_hash
+    GEMM kernel source, or None (no capture, or the source changed since)."""
+    from shape_adaptive_tile_gb300.build import gemm_source_hash
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     key = desc.split(":")[0].strip()
-    cur = source_hash()
+    cur = gemm_source_hash()
     with open(path) as f:
         for line in f:
             if line.startswith("#") or "|" not in line:

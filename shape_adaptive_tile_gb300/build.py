@@ -50,6 +50,23 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+# Sources of the row operators only: no GEMM kernel includes or calls them.
+_ROWOP_ONLY = ("rowops.cu", "rowops.h")
+
+
+def gemm_source_hash() -> str:
+    """SHA-256 of the sources the GEMM kernels are built from: every input but
+    the row operators' own files. A profile of a GEMM kernel stays valid as
+    long as this is unchanged."""
+    h = hashlib.sha256()
+    for f in _inputs():
+        if os.path.basename(f) in _ROWOP_ONLY:
+            continue
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
 def _key(nvcc: str) -> str:
     ver = subprocess.run([nvcc, "--version"], capture_output=True, text=True, check=True).stdout
     h = hashlib.sha256()
