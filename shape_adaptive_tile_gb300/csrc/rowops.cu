@@ -89,9 +89,23 @@ __global__ void __launch_bounds__(NT)
             }
         }
     };
+    // Rows of 4-byte elements (up to 16 per thread): gamma and beta are read
+    // into registers right after the row, so their latency overlaps the
+    // row's instead of following the reductions one column at a time.
+    constexpr bool kEarly = VEC == 1 && PER <= 16 && OP != kSoftmax;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         float v[PER];
         load_row(v, r);
+        float ge[kEarly ? PER : 1], be[kEarly && OP == kLayerNorm ? PER : 1];
+        if constexpr (kEarly) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int c = i * NT + threadIdx.x;
+                ge[i] = gamma && c < width ? gamma[c] : 1.0f;
+                if constexpr (OP == kLayerNorm)
+                    be[i] = beta && c < width ? beta[c] : 0.0f;
+            }
+        }
         auto valid = [&](int i) { return (i / VEC * NT + threadIdx.x) * VEC + i % VEC < width; };
         float scale = 0.0f, shift = 0.0f;
         if constexpr (OP == kSoftmax) {
@@ -144,7 +158,11 @@ __global__ void __launch_bounds__(NT)
                 gv[e] = 1.0f;
                 bv[e] = 0.0f;
             }
-            if constexpr (OP != kSoftmax) {
+            if constexpr (kEarly) {
+                gv[0] = ge[i];
+                if constexpr (OP == kLayerNorm)
+                    bv[0] = be[i];
+            } else if constexpr (OP != kSoftmax) {
                 if (gamma) {
                     if constexpr (VEC == 4) {
                         const float4 q = *reinterpret_cast<const float4*>(gamma + c);
