@@ -141,3 +141,25 @@ def test_dispatcher_rejects_bad_arguments():
         sat.gemm_select_config(-1, 4, 4, "tf32", 152, True)
     with pytest.raises(sat.GemmError):
         sat.gemm_select_config(4, 4, 4, "tf32", 0, True)
+
+
+def test_gemm_source_hash_ignores_only_the_row_operators(tmp_path, monkeypatch):
+    # The recorded GEMM traffic is keyed on this hash: editing a row-operator
+    # file must leave it alone, editing a GEMM source must change it.
+    from shape_adaptive_tile_gb300 import build as b
+    src = tmp_path / "csrc"
+    inc = tmp_path / "include"
+    src.mkdir()
+    inc.mkdir()
+    for name in ("gemm_kernel.cuh", "rowops.cu", "api.cu"):
+        (src / name).write_text(name)
+    for name in ("gemm.h", "rowops.h"):
+        (inc / name).write_text(name)
+    monkeypatch.setattr(b, "CSRC", str(src))
+    monkeypatch.setattr(b, "INCLUDE", str(inc))
+    h0, f0 = b.gemm_source_hash(), b.source_hash()
+    (src / "rowops.cu").write_text("changed")
+    (inc / "rowops.h").write_text("changed")
+    assert b.gemm_source_hash() == h0 and b.source_hash() != f0
+    (src / "gemm_kernel.cuh").write_text("changed")
+    assert b.gemm_source_hash() != h0
