@@ -146,7 +146,8 @@ def test_dispatcher_rejects_bad_arguments():
 def test_gemm_source_hash_ignores_only_the_row_operators(tmp_path, monkeypatch):
     # The recorded GEMM traffic is keyed on this hash: editing a row-operator
     # file must leave it alone, editing a GEMM source must change it.
-    from shape_adaptive_tile_gb300 import build as b
+    import importlib
+    b = importlib.import_module("shape_adaptive_tile_gb300.build")
     src = tmp_path / "csrc"
     inc = tmp_path / "include"
     src.mkdir()
