@@ -93,7 +93,7 @@ def test_rowop_matches_oracle_and_repeats(op, rows, width):
 
 
 @pytest.mark.parametrize("op", si.ROWOPS)
-@pytest.mark.parametrize("width", [1, 3, 4, 513, 2048, 16385, 32768])
+@pytest.mark.parametrize("width", [1, 3, 4, 513, 2048, 2052, 3000, 4100, 6000, 8188, 16385, 32768])
 def test_rowop_widths_and_tails(op, width):
     x, g, b = si.rowop_inputs(5, width, seed=7)
     got = _device_run(op, x, g, b).cpu().numpy()
@@ -101,21 +101,22 @@ def test_rowop_widths_and_tails(op, width):
 
 
 @pytest.mark.parametrize("op", si.ROWOPS)
-def test_rowop_strided_and_in_place(op):
-    rows, width = 9, 1000
+@pytest.mark.parametrize("width,ldx,ldy", [(1000, 1100, 1024), (3000, 3100, 3072), (6000, 6004, 6144)])
+def test_rowop_strided_and_in_place(op, width, ldx, ldy):
+    rows = 9
     x, g, b = si.rowop_inputs(rows, width, seed=8)
     ref = _reference(op, x, g, b)
-    # strided: rows 1100 apart in X, 1024 apart in Y; padding must stay untouched
-    xs = np.full((rows, 1100), np.nan, np.float32)
+    # strided: rows ldx apart in X, ldy apart in Y; padding must stay untouched
+    xs = np.full((rows, ldx), np.nan, np.float32)
     xs[:, :width] = x
-    ys = torch.full((rows, 1024), -7.0, device="cuda")
+    ys = torch.full((rows, ldy), -7.0, device="cuda")
     dx = torch.from_numpy(xs).cuda()
     if op == "softmax":
-        rc = sat.rowop_softmax(dx, 1100, ys, 1024, rows, width, stream())
+        rc = sat.rowop_softmax(dx, ldx, ys, ldy, rows, width, stream())
     elif op == "rmsnorm":
-        rc = sat.rowop_rmsnorm(dx, 1100, torch.from_numpy(g).cuda(), ys, 1024, rows, width, 1e-5, stream())
+        rc = sat.rowop_rmsnorm(dx, ldx, torch.from_numpy(g).cuda(), ys, ldy, rows, width, 1e-5, stream())
     else:
-        rc = sat.rowop_layernorm(dx, 1100, torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda(), ys, 1024, rows,
+        rc = sat.rowop_layernorm(dx, ldx, torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda(), ys, ldy, rows,
                                  width, 1e-5, stream())
     assert rc == 0, sat.gemm_last_error()
     torch.cuda.synchronize()
