@@ -213,18 +213,19 @@ template <int OP, int VEC>
 cudaError_t launch_vec(const float* X, int64_t ldx, const float* g, const float* b, float* Y, int64_t ldy,
                        int64_t rows, int width, float eps, cudaStream_t s)
 {
-    // Rows of 16-byte vectors from 513 to 8192 columns: fewer threads per
-    // row, each holding more of it. That spreads the per-row work (the
+    // Rows of 16-byte vectors up to 8192 columns: fewer threads per row,
+    // each holding more of it. That spreads the per-row work (the
     // reductions, the scale, the index arithmetic) over more elements and
     // keeps more loads in flight per thread; the thread counts are the
-    // fastest measured per operator on GB300 (rows x 1024, 2048, 4096 and
-    // 8192).
+    // fastest measured per operator on GB300 (rows x 256 to x 8192).
     if constexpr (VEC == 4) {
-        if (width > 512 && width <= 1024)
+        if (width <= 512)
+            return launch_one<OP, 128, 4, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
+        if (width <= 1024)
             return launch_one<OP, 128, 8, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-        if (width > 1024 && width <= 2048)
+        if (width <= 2048)
             return launch_one<OP, 128, 16, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
-        if (width > 2048 && width <= 4096) {
+        if (width <= 4096) {
             if constexpr (OP == kLayerNorm)
                 return launch_one<OP, 128, 32, VEC>(X, ldx, g, b, Y, ldy, rows, width, eps, s);
             else
