@@ -170,22 +170,27 @@ int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* 
  * Computes the same C = alpha * A * B + beta * C as gemm_run, with the same
  * arguments, conventions, alignment rules and the dispatcher's choice of
  * kernel, but makes no plan and calls no cudaMalloc, cudaFree or other
- * allocating routine. The kernel's scratch memory (a status word and, when K
- * is split, the partial tiles) is one fixed 16 MiB device array inside the
- * library, which every GPU that loads the library holds until the process
- * exits.
- *   - A problem whose split-K partial tiles need more than that array holds
- *     (splits x M rounded up to the tile height x N floats > 16 MiB - 256
- *     bytes; e.g. bf16 128 x 19456 x 8192, split 2 ways) is rejected with
- *     GEMM_ERR_ARG and a message saying so; gemm_run serves it.
+ * allocating routine. The kernel's scratch memory is one fixed 32 MiB
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits. Its first 4 KiB hold the status word
+ * (offset 0) and the stream-K counters (from offset 256: at most 960, one
+ * per CTA of the grid); the other 32 MiB - 4 KiB hold the split-K partial
+ * tiles (splits x M rounded up to the tile height, 128 or 256 rows, x N
+ * floats) or the stream-K partial tiles (one 128 x bn float tile per CTA).
+ *   - A problem whose partial tiles or counters would not fit is rejected
+ *     with GEMM_ERR_ARG and a message naming the limit; gemm_run serves it.
+ *     On a 152-SM GB300 no choice of the dispatcher comes near either limit
+ *     (its K splits and stream-K grids keep the partial tiles within one
+ *     128 x 256 float tile per SM, 19.9 MB), so the check guards devices
+ *     with more SMs.
  *   - The first call on each device looks up the array's address on that
  *     device (so the device must be current); make that first call before
  *     any CUDA stream capture.
  *   - Every call shares the array, which keeps the previous call's contents;
- *     the status word is cleared on the stream at the start of each call.
- *     Calls whose kernels overlap on the GPU (different streams, or the same
- *     stream from several threads without ordering) race on the array and may
- *     produce wrong results: order them.
+ *     the status word and the counters are cleared on the stream at the
+ *     start of each call. Calls whose kernels overlap on the GPU (different
+ *     streams, or the same stream from several threads without ordering)
+ *     race on the array and may produce wrong results: order them.
  *   - A bounded wait that gives up inside the kernel still ends it; this
  *     entry point has no status query (plans have gemm_plan_status).
  * Returns 0 after enqueueing on `cuda_stream`, or a negative gemm_status_t

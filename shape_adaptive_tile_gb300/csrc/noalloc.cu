@@ -7,9 +7,10 @@
 // allocates (host state, an error word and, for split-K plans, a workspace),
 // so such callers use this entry point instead. It needs no plan: the
 // dispatcher's choice, the tensor maps and the launch parameters live on the
-// stack, and the kernel's scratch memory (its status word and the split-K
-// partial tiles) lives in one file-scope device array of fixed size that
-// every GPU loading this library holds until the process exits.
+// stack, and the kernel's scratch memory (its status word, the stream-K
+// counters, and the split-K or stream-K partial tiles) lives in one
+// file-scope device array of fixed size that every GPU loading this library
+// holds until the process exits.
 #include "gemm.h"
 
 #include <cuda.h>
@@ -178,11 +179,16 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
         if (sat::sk_layout(tiles, num_kb, slots, &sk_tiles, &sk_w)) {
             sk_ctas = slots * k->cg;
             const size_t need = static_cast<size_t>(sk_ctas) * 128 * k->bn * 4;
-            if (need > kWorkspaceBytes || kCounterOffset + static_cast<size_t>(sk_ctas) * 4 > kStatusBytes)
+            if (need > kWorkspaceBytes)
                 return sat::fail_with(GEMM_ERR_ARG,
                             "this problem's stream-K partial tiles need %zu bytes of scratch; the allocation-free "
                             "entry point has %zu bytes (use gemm_plan_create/gemm_run)",
                             need, kWorkspaceBytes);
+            if (kCounterOffset + static_cast<size_t>(sk_ctas) * 4 > kStatusBytes)
+                return sat::fail_with(GEMM_ERR_ARG,
+                            "this problem's stream-K grid has %lld CTAs, each needing a counter; the "
+                            "allocation-free entry point has %zu counter slots (use gemm_plan_create/gemm_run)",
+                            static_cast<long long>(sk_ctas), (kStatusBytes - kCounterOffset) / 4);
         }
     }
     e = k->prepare();

@@ -164,3 +164,28 @@ def test_gemm_source_hash_ignores_only_the_row_operators(tmp_path, monkeypatch):
     assert b.gemm_source_hash() == h0 and b.source_hash() != f0
     (src / "gemm_kernel.cuh").write_text("changed")
     assert b.gemm_source_hash() != h0
+
+
+def test_noalloc_scratch_holds_every_dispatcher_choice_on_a_gb300():
+    # gemm_run_noalloc keeps its partial tiles in a fixed array of 32 MiB
+    # minus a 4 KiB status area (status word, then one stream-K counter per
+    # CTA from byte 256). On a 152-SM GB300 every choice of the dispatcher
+    # must fit, from skinny to square, short K to long: its K splits and
+    # stream-K grids keep the partial tiles within one 128 x 256 float tile
+    # per SM.
+    sms, limit, counters = 152, (32 << 20) - 4096, (4096 - 256) // 4
+    worst = 0
+    for dt in ("tf32", "bf16", "fp16"):
+        for M in (1, 16, 32, 100, 128, 129, 256, 300, 1000, 2048, 4096, 8191, 16384, 65536):
+            for N in (8, 256, 1000, 4096, 8192, 19456, 65536):
+                for K in (64, 512, 2049, 8192, 65536):
+                    f = sat.gemm_select_config(M, N, K, dt, sms, True).split(",")
+                    bn, cg, splits, sk = int(f[0]), int(f[1]), int(f[4]), int(f[6])
+                    rows = 128 * cg
+                    need = splits * (-(-M // rows) * rows) * N * 4 if splits > 1 else 0
+                    if sk:
+                        need = max(need, (sms // cg) * cg * 128 * bn * 4)
+                        assert (sms // cg) * cg <= counters
+                    worst = max(worst, need)
+                    assert need <= limit, (dt, M, N, K, f, need)
+    assert 0 < worst <= sms * 128 * 256 * 4
