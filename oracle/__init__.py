@@ -126,6 +126,40 @@ def gemm(A, B, C0=None, alpha=1.0, beta=0.0, dtype="tf32", row_begin=0, row_end=
     return out64, out32
 
 
+def _exact_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """The exact values of stored operand elements as doubles: fp32 and fp16
+    widen exactly; a bf16 bit pattern is the top half of the fp32 with the
+    same sign, exponent and leading fraction bits."""
+    code = _code(dtype)
+    if code == 1:
+        return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def gemm_full(A, B, C0=None, alpha=1.0, beta=0.0, dtype="tf32"):
+    """All of alpha*A*B + beta*C0 in double, with numpy's float64 matrix
+    product as the sum over k; returns (f64, f32).
+
+    The same definition as :func:`gemm`, with a library matrix product as
+    its one step: the operands enter as the exact doubles of their stored
+    bits, ``acc = A @ B`` in float64, ``out64 = alpha*acc + beta*C0`` (the
+    beta term only when beta != 0), ``out32`` one round to nearest even.
+    The library sums over k in its own blocked order, so ``out64`` can differ
+    from :func:`gemm`'s ascending-k double sum by a few units in the last
+    place of double; where every partial sum is exact in double (the dyadic
+    family) both are exact and equal bit for bit. It exists for complete
+    outputs of the largest benchmark shapes, where the plain loop streams B
+    from memory once per row of A.
+    """
+    A, B, C0, M, N, K = _prep(A, B, C0, beta, dtype)
+    acc = _exact_f64(A, dtype) @ _exact_f64(B, dtype) if K > 0 else np.zeros((M, N))
+    out64 = float(alpha) * acc
+    del acc
+    if beta != 0.0:
+        out64 += float(beta) * C0.astype(np.float64)
+    return out64, out64.astype(np.float32)
+
+
 def gemm_entries(A, B, rows, cols, C0=None, alpha=1.0, beta=0.0, dtype="tf32"):
     """Entries (rows[e], cols[e]) of alpha*A*B + beta*C0; returns (f64, f32)."""
     A, B, C0, M, N, K = _prep(A, B, C0, beta, dtype)

@@ -330,3 +330,77 @@ def test_oracle_uses_unrounded_fp32_not_tf32():
     a = np.array([[1.0 + 2.0 ** -20]], dtype=np.float32)
     c64, _ = oracle.gemm(a, np.array([[1.0]], np.float32))
     assert c64[0, 0] == 1.0 + 2.0 ** -20
+
+
+# --- the full-output form (numpy's float64 product as the sum over k) ---------
+
+def test_full_form_decodes_every_bf16_and_fp16_pattern():
+    # A column of every finite pattern times [[1]] returns each value exactly.
+    for dtype in ("bf16", "fp16"):
+        bits = np.arange(1 << 16, dtype=np.uint32)
+        want = np.array([oracle.decode(dtype, int(b)) for b in bits])
+        keep = np.isfinite(want)
+        col = bits[keep].astype(np.uint16).reshape(-1, 1)
+        if dtype == "fp16":
+            col = col.view(np.float16)
+        one = _exact(dtype, [1.0]).reshape(1, 1)
+        c64, _ = oracle.gemm_full(col, one, dtype=dtype)
+        assert np.array_equal(c64[:, 0], want[keep])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_full_form_closed_forms(dtype):
+    A = si.matrix("dyadic", dtype, 13, 9, 11, 0)
+    I9 = _exact(dtype, np.eye(9)).reshape(9, 9)
+    dec = (lambda x: si.bf16_bits_to_f32(x)) if dtype == "bf16" else (lambda x: x)
+    c64, _ = oracle.gemm_full(A, I9, dtype=dtype)
+    assert np.array_equal(c64, dec(A).astype(np.float64))
+    K = 777
+    ones_a = _exact(dtype, np.ones(3 * K)).reshape(3, K)
+    ones_b = _exact(dtype, np.ones(K * 5)).reshape(K, 5)
+    c64, c32 = oracle.gemm_full(ones_a, ones_b, dtype=dtype)
+    assert np.all(c64 == K) and np.all(c32 == K)
+    u = si.matrix("dyadic", dtype, 23, 1, 2, 0)
+    v = si.matrix("dyadic", dtype, 1, 19, 2, 1)
+    c64, _ = oracle.gemm_full(u, v, dtype=dtype)
+    assert np.array_equal(c64, np.outer(dec(u).astype(np.float64), dec(v).astype(np.float64)))
+
+
+def test_full_form_alpha_beta_terms():
+    A, B, C0 = si.problem(9, 11, 5, "tf32", "dyadic", 8, "dyadic")
+    ab, _ = oracle.gemm_full(A, B)
+    c64, _ = oracle.gemm_full(A, B, C0, 1.5, -0.5)
+    assert np.array_equal(c64, 1.5 * ab - 0.5 * C0.astype(np.float64))
+    c64, _ = oracle.gemm_full(A, B, C0, 0.0, 0.75)
+    assert np.array_equal(c64, 0.75 * C0.astype(np.float64))
+    nan = np.full((9, 11), np.nan, np.float32)
+    c64, c32 = oracle.gemm_full(A, B, nan, 2.0, 0.0)
+    assert np.array_equal(c64, 2.0 * ab) and np.all(np.isfinite(c32))
+    c64, _ = oracle.gemm_full(np.zeros((3, 0), np.float32), np.zeros((0, 4), np.float32), C0[:3, :4], 2.0, 0.5)
+    assert np.array_equal(c64, 0.5 * C0[:3, :4].astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_full_form_equals_plain_loop_bit_for_bit_on_dyadic(dtype):
+    # Every partial sum is exact in double, so any summation order gives the
+    # same bits; non-square ragged shapes catch a transposed operand.
+    for M, N, K in ((1, 1, 1), (37, 53, 41), (130, 7, 300), (5, 260, 1031)):
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 30 + M, "dyadic")
+        f64, f32 = oracle.gemm_full(A, B, C0, 1.5, 0.5, dtype)
+        g64, g32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        assert np.array_equal(f64, g64) and np.array_equal(f32.view(np.uint32), g32.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_full_form_close_to_plain_loop_on_gaussian(dtype):
+    M, N, K = 67, 45, 2050
+    A, B, C0 = si.problem(M, N, K, dtype, "normal", 40, "normal")
+    f64, f32 = oracle.gemm_full(A, B, C0, 1.25, -0.5, dtype)
+    g64, g32 = oracle.gemm(A, B, C0, 1.25, -0.5, dtype)
+    dec = (lambda x: si.bf16_bits_to_f32(x)) if dtype == "bf16" else (lambda x: x)
+    scale = 1.25 * (np.abs(dec(A).astype(np.float64)) @ np.abs(dec(B).astype(np.float64))) + 0.5 * np.abs(C0)
+    assert np.all(np.abs(f64 - g64) <= 1e-13 * scale)
+    assert oracle.rel_rms(f64, g64) < 1e-14
+    # A few double ulps apart, the two round to the same floats (a tie within
+    # that distance has probability of order 1e-9 per element).
+    assert np.array_equal(f32.view(np.uint32), g32.view(np.uint32))
