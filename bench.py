@@ -3,8 +3,10 @@
 
 One step = one GEMM C = alpha*A*B + beta*C through the C ABI on one batch
 of seeded synthetic inputs (the whole hot path). The default workload is
-the TF32 2048^3 GEMM with N(0,1) inputs (alpha 1, beta 0, seed 1); the
-metric is TFLOP/s = 2*M*N*K / t.
+the largest configuration, the TF32 8192^3 GEMM with N(0,1) inputs (alpha 1,
+beta 0, seed 2), in the regime where the dense-peak target applies; the
+metric is TFLOP/s = 2*M*N*K / t. Every other configuration is one
+--workload away.
 
 Timing: W untimed warm-up steps, then exactly K timed steps between a
 barrier + device synchronisation on both sides. Each step writes a 256 MiB
@@ -28,6 +30,7 @@ import csv
 import io
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -43,7 +46,7 @@ import synth_inputs as si  # noqa: E402
 
 METRIC = "GEMM TFLOP/s (2MNK/t) per dtype/shape; % of GB300 dense tensor peak"
 UNIT = "TFLOP/s"
-DEFAULT = "tf32-square2048"
+DEFAULT = "tf32-square8192"
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp16": 2250.0, "tf32": 1100.0}
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
@@ -80,32 +83,92 @@ def min_bytes(dtype, M, N, K, beta):
 
 
 # ----------------------------------------------------------------- clocks
+_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and clock-event reasons sampled every ~2 ms while running,
+    read through NVML (the driver's libnvidia-ml; reading only), or from
+    nvidia-smi every 50 ms when NVML cannot be loaded."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.002):
         self.index = index
+        self.period = period_s
         self.proc = None
-        self.rows = []
+        self.nvml = None
+        self.rows = []          # (time, sm_mhz, max_mhz, set of reasons)
+        self.source = None
         self.t_start = self.t_stop = None
+        self._stop = threading.Event()
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return False
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mhz, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) != 0:
+            return False
+        self.max_mhz = float(mhz.value)
+
+        def sample():
+            if lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) != 0:
+                return None
+            r = set()
+            if get_reasons(h, ctypes.byref(bits)) == 0:
+                r = {n for n, b in _REASON_BITS.items() if bits.value & b}
+            return float(mhz.value), r
+
+        self.nvml = (lib, sample)
+        return True
 
     def start(self):
+        try:
+            ok = self._open_nvml()
+        except (OSError, AttributeError):
+            ok = False
+        if ok:
+            self.source = f"NVML, every {self.period * 1e3:g} ms"
+            self.reader = threading.Thread(target=self._poll, daemon=True)
+            self.reader.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, every 50 ms"
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except OSError:
             self.proc = None
 
+    def _poll(self):
+        _, sample = self.nvml
+        while not self._stop.is_set():
+            v = sample()
+            if v is not None:
+                self.rows.append((time.time(), v[0], self.max_mhz, v[1]))
+            time.sleep(self.period)
+
     def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.rows.append((time.time(), line.strip()))
+            for row in csv.reader(io.StringIO(line.strip())):
+                try:
+                    r = {n for n, v in zip(names, row[5:9]) if v.strip().lower() == "active"}
+                    self.rows.append((time.time(), float(row[1]), float(row[2]), r))
+                except (ValueError, IndexError):
+                    continue
 
     def mark(self, start):
         if start:
@@ -114,6 +177,7 @@ class ClockSampler:
             self.t_stop = time.time()
 
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -123,22 +187,35 @@ class ClockSampler:
 
     def summary(self):
         if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        inside = [r for t, r in self.rows if self.t_start and self.t_start <= t <= (self.t_stop or t)]
-        use = inside or [r for _, r in self.rows]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for row in csv.reader(io.StringIO("\n".join(use))):
-            try:
-                sm.append(float(row[1]))
-                smax.append(float(row[2]))
-                for n, v in zip(names, row[5:9]):
-                    if v.strip().lower() == "active":
-                        reasons.add(n)
-            except (ValueError, IndexError):
-                continue
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": len(inside)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples (NVML and nvidia-smi unavailable)"],
+                    "samples": 0, "samples_in_timed_region": 0}
+        inside = [r for r in self.rows if self.t_start and self.t_start <= r[0] <= (self.t_stop or r[0])]
+        use = inside or self.rows
+        sm = [r[1] for r in use]
+        reasons = set().union(*(r[3] for r in use))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[2] for r in use),
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "samples": len(self.rows),
+                "samples_in_timed_region": len(inside), "source": self.source}
+
+
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo or lscpu), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
 
 
 # ----------------------------------------------------------------- oracle arm
@@ -188,7 +265,7 @@ def run_reference(args, w, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe_workload(w), "name": args.workload},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {what}"},
+                         "sample": f"per step: {what}", "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -307,13 +384,16 @@ def bench_one(args, w, rank, world, torch, sat, quiet=False):
     torch.cuda.synchronize()
     if clocks:
         clocks.mark(True)
+    # Kernels per gemm_run: the GEMM, plus the fixed-order reduction when the
+    # plan splits K ("s<splits>" in its description).
+    per_run = 2 if re.search(r" s([2-9]|1[0-6]) ", desc) else 1
     launches = 0
     for e0, e1 in ev:
         flush.zero_()
         e0.record(stream)
         plan.run(dA, dB, dC, alpha, beta, sptr)
         e1.record(stream)
-        launches += 1
+        launches += per_run
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -435,7 +515,10 @@ def main():
         "config": {"workload": describe_workload(w), "name": args.workload, "M": r["M"], "N": r["N"],
                    "K": r["K"], "plan": r["plan"], "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (256 MiB write outside the timed events)",
-                   "median_ms": statistics.median(r["times_ms"]), "min_ms": min(r["times_ms"])},
+                   "median_ms": statistics.median(r["times_ms"]), "min_ms": min(r["times_ms"]),
+                   "p90_ms": sorted(r["times_ms"])[int(0.9 * (len(r["times_ms"]) - 1))],
+                   "samples": len(r["times_ms"]),
+                   "value_from": "steps x 2MNK / sum of the step times (CUDA events around each gemm_run)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic_for(r["plan"]),
                      "peak_source": f"{pk_src}: bf16 burst {pk['bf16_tflops']} TFLOP/s x "
@@ -447,7 +530,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tflops, cores, what, secs = oracle_sample(w, 12.0)
         line["cpu_baseline"] = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{what}, {secs:.1f} s"}
+                                "sample": f"{what}, {secs:.1f} s", "cpu": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

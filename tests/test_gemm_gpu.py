@@ -315,3 +315,51 @@ def test_plan_runs_on_two_streams():
         torch.cuda.synchronize()
     for c in outs:
         checks.assert_bit_exact(c.cpu().numpy(), ref32, "two streams")
+
+
+# TF32 operand conversion: the pages do not say whether the tensor core
+# truncates an fp32 operand to TF32's 10 fraction bits or rounds it. Probe it
+# with values whose low fraction bits decide: each output is one product
+# v * 1 (the other K terms are zero), exact in the fp32 accumulator, so it
+# shows the operand as the tensor core used it. The oracle keeps the full
+# fp32 value; any of these readings stays inside the rel_rms gate.
+_PROBES = np.array([1 + 2.0 ** -11 + 2.0 ** -12, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11,
+                    -(1 + 2.0 ** -11 + 2.0 ** -12)], dtype=np.float64)
+_READINGS = {
+    "truncate": np.array([1.0, 1.0, 1 + 2.0 ** -10, -1.0]),
+    "nearest, ties away": np.array([1 + 2.0 ** -10, 1 + 2.0 ** -10, 1 + 2.0 ** -9, -(1 + 2.0 ** -10)]),
+    "nearest, ties even": np.array([1 + 2.0 ** -10, 1.0, 1 + 2.0 ** -9, -(1 + 2.0 ** -10)]),
+    "full fp32": _PROBES,
+}
+
+
+def _conversion(got):
+    for name, want in _READINGS.items():
+        if np.array_equal(got.astype(np.float64), want):
+            return name
+    return None
+
+
+@pytest.mark.parametrize("config", [None, "128,1,0,1", "128,1,0,1,plain", "256,2,0,1"])
+def test_tf32_operand_conversion(config):
+    P = len(_PROBES)
+    M, N, K = 256, 256, 64     # the probes in row i < P of A (column 0); B[0, :] = 1
+    A = np.zeros((M, K), np.float32)
+    A[:P, 0] = _PROBES
+    B = np.zeros((K, N), np.float32)
+    B[0, :] = 1.0
+    got_a, desc_a = run_np(M, N, K, "tf32", A, B, None, 1.0, 0.0, config)
+    # and the same probes in B (row 0, columns j < P), A[:, 0] = 1
+    A2 = np.zeros((M, K), np.float32)
+    A2[:, 0] = 1.0
+    B2 = np.zeros((K, N), np.float32)
+    B2[0, :P] = _PROBES
+    got_b, desc_b = run_np(M, N, K, "tf32", A2, B2, None, 1.0, 0.0, config)
+    ra, rb = _conversion(got_a[:P, 0]), _conversion(got_b[0, :P])
+    print(f"tf32 operand conversion [{desc_a}]: A {ra}, B {rb}")
+    assert ra is not None and rb is not None, (got_a[:P, 0], got_b[0, :P])
+    assert ra == rb, "A and B operands converted differently"
+    # Measured on GB300: the tensor core truncates both operands to TF32 on
+    # every load path (the dropped bits bias each product toward zero by
+    # about 7e-4 relative on N(0,1) data, inside the 1e-3 rel_rms gate).
+    assert ra == "truncate"
