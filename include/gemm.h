@@ -61,13 +61,15 @@ typedef enum {
 /*
  * Choose the kernel (tile shape, CTA-pair or single SM, stage count, raster
  * order, load path) for this problem on the CURRENT device, and prepare it.
- * M, N, K >= 0 and each < 2^31. Allocates host state and one 4-byte device
- * error word, both owned by the plan, and, when the choice splits K, a device
- * workspace of splits x ceil(M/256)*256 x N floats for the partial tiles;
- * for a stream-K choice, one 128 x bn float partial tile and one counter
- * per CTA of the grid (at most one per SM).
- * Returns NULL on failure; the reason is in gemm_last_error(). Must not be
- * called during CUDA stream capture.
+ * M, N, K >= 0 and each < 2^31. Allocates host state and a 64-byte
+ * host-mapped pinned error word, both owned by the plan. A plan whose choice
+ * splits K, or cuts the last waves of tiles into stream-K pieces, also owns
+ * device scratch for its partial tiles, one set per stream it runs on (at
+ * most 8 sets), allocated by the first run on each stream: a split-K set is
+ * splits x ceil(M/256)*256 x N floats; a stream-K set one 128 x bn float
+ * partial tile and one counter per CTA of the grid (at most one per SM),
+ * plus a slot ticket. Returns NULL on failure; the reason is in
+ * gemm_last_error(). Must not be called during CUDA stream capture.
  */
 gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype);
 
@@ -122,14 +124,20 @@ gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
  * strides take the TMA load path, anything else the plain-load path, with
  * identical results. A plan that splits K launches a second kernel on the
  * same stream that sums the partial tiles in fixed order and applies alpha
- * and beta; its workspace is then in use until that kernel ends, so runs of
- * such a plan on different streams must be ordered by the caller. A
- * stream-K plan's CTAs wait (bounded) for each other's partial tiles inside
- * one launch, so it needs its whole grid resident: runs of such a plan must
- * not overlap each other or other work that holds SMs for long. Other plans
- * are read-only here and may run on several streams or threads at once. Launch failures return
- * GEMM_ERR_LAUNCH; kernel-side bounded-wait timeouts are reported by
- * gemm_plan_status().
+ * and beta.
+ * Threading: one plan may run on several streams, from several threads, at
+ * once. A split-K or stream-K plan keeps its partial tiles in scratch of the
+ * stream's own (allocated by the plan's first run on that stream, so make
+ * that first run before any stream capture; past 8 streams, a new stream
+ * takes over the set used least recently, ordered behind that set's last
+ * run by an event wait on the GPU). Stream-K CTAs wait for partial tiles
+ * only of CTAs that started before them (slots are handed out in start
+ * order), so such runs finish whether or not the whole grid is resident,
+ * beside each other or beside other work.
+ * Errors: launch failures return GEMM_ERR_LAUNCH. A kernel of this plan that
+ * gave up a bounded wait marks the plan's host-mapped error word; the next
+ * gemm_run of the plan sees it without synchronising and returns
+ * GEMM_ERR_TIMEOUT with nothing enqueued, until gemm_plan_status() clears it.
  */
 int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, float alpha, float beta,
              void* cuda_stream);
@@ -173,8 +181,9 @@ int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* 
  * allocating routine. The kernel's scratch memory is one fixed 32 MiB
  * device array inside the library, which every GPU that loads the library
  * holds until the process exits. Its first 4 KiB hold the status word
- * (offset 0) and the stream-K counters (from offset 256: at most 960, one
- * per CTA of the grid); the other 32 MiB - 4 KiB hold the split-K partial
+ * (offset 0), the stream-K slot ticket (offset 128) and the stream-K
+ * counters (from offset 256: at most 960, one per CTA of the grid); the
+ * other 32 MiB - 4 KiB hold the split-K partial
  * tiles (splits x M rounded up to the tile height, 128 or 256 rows, x N
  * floats) or the stream-K partial tiles (one 128 x bn float tile per CTA).
  *   - A problem whose partial tiles or counters would not fit is rejected
@@ -187,7 +196,7 @@ int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* 
  *     device (so the device must be current); make that first call before
  *     any CUDA stream capture.
  *   - Every call shares the array, which keeps the previous call's contents;
- *     the status word and the counters are cleared on the stream at the
+ *     the status word, the ticket and the counters are cleared on the stream at the
  *     start of each call. Calls whose kernels overlap on the GPU (different
  *     streams, or the same stream from several threads without ordering)
  *     race on the array and may produce wrong results: order them.
@@ -199,12 +208,15 @@ int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* 
 int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const void* A, const void* B, float* C,
                      float alpha, float beta, void* cuda_stream);
 
-/* Free the plan and its device error word. NULL is accepted. Synchronises
- * nothing: do not destroy a plan whose runs may still be executing. */
+/* Free the plan, its error word and its scratch. NULL is accepted.
+ * Synchronises nothing: do not destroy a plan whose runs may still be
+ * executing. */
 void gemm_plan_destroy(gemm_plan* plan);
 
 /*
- * Synchronise the device, read and clear the plan's device error word.
+ * Synchronise the device, read and clear the plan's error word (and, if it
+ * was set, clear the stream-K counters of every scratch set, whose numbering
+ * a launch that gave up may have left short).
  * Returns 0 if no kernel of this plan gave up a bounded wait since the last
  * call, GEMM_ERR_TIMEOUT if one did, GEMM_ERR_LAUNCH if the device reported
  * an error.

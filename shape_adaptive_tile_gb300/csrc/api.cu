@@ -11,7 +11,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
-#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -75,6 +74,31 @@ int fail_with(int code, const char* fmt, ...)
 }
 }  // namespace sat
 
+namespace {
+
+// Device scratch that the runs of a split-K or stream-K plan write: the
+// split-K partial tiles, or the stream-K partial tiles, counters and slot
+// ticket. One set per stream the plan runs on, so that runs on different
+// streams never share them; the stream's own order keeps runs on one stream
+// apart. At most kMaxScratch sets per plan: past that, a new stream takes
+// over the set used least recently, behind that set's last run (a wait on
+// the GPU for the event recorded after it, not on the host).
+struct Scratch {
+    unsigned long long stream_id = 0;  // cudaStreamGetId of the stream that uses it
+    float* ws = nullptr;               // split-K: splits x ws_rows x N floats
+    CUtensorMap tmW{};                 // ws for the bulk-store epilogue
+    bool ws_tma = false;
+    float* sk_ws = nullptr;            // stream-K: one 128 x bn float partial tile per CTA
+    unsigned* sk_flags = nullptr;      // stream-K: one counter per CTA, then the ticket counter
+    unsigned epoch = 0;                // stream-K launches on these counters since they were cleared
+    cudaEvent_t done = nullptr;        // recorded after each run that used this set
+    unsigned long long last_use = 0;
+};
+constexpr int kMaxScratch = 8;
+constexpr int kTicketPad = 32;  // the ticket counter sits 128 bytes past the last CTA counter
+
+}  // namespace
+
 struct gemm_plan {
     int64_t M = 0, N = 0, K = 0;
     int dt = 0;
@@ -89,19 +113,20 @@ struct gemm_plan {
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
     const sat::KernelEntry* plain_strided = nullptr;  // the same, for row strides other than K and N
     int grid_tma = 0, grid_plain = 0;
+    // Error word in host-mapped pinned memory: kernels OR bits into it through
+    // d_err; the host reads h_err without synchronising.
+    uint32_t* h_err = nullptr;
     uint32_t* d_err = nullptr;
-    // Split-K: `splits` slices of `ws_rows` x N floats in `ws`, reduced in
-    // fixed order into C; tmW describes ws for the bulk-store epilogue.
+    // Split-K: `splits` slices of `ws_rows` x N floats, reduced in fixed order
+    // into C (the slices live in the per-stream scratch).
     int splits = 1, kb_per_split = 0, ws_rows = 0;
-    float* ws = nullptr;
-    bool ws_tma = false;
-    CUtensorMap tmW{};
-    // Stream-K (the choice's sk): layout, one 128 x BN partial tile and one
-    // counter per CTA, and the launch number the counters are compared with.
-    int sk_tiles = 0, sk_w = 0, sk_ctas = 0;
-    float* sk_ws = nullptr;
-    unsigned* sk_flags = nullptr;
-    mutable std::atomic<unsigned> sk_epoch{0};
+    // Stream-K (the choice's sk): layout, and per-stream scratch of one
+    // 128 x BN partial tile and one counter per CTA.
+    int sk_tiles = 0, sk_w = 0, sk_ctas = 0, sk_bn = 0;
+    mutable std::mutex scratch_mu;
+    mutable Scratch scratch[kMaxScratch];
+    mutable int n_scratch = 0;
+    mutable unsigned long long use_clock = 0;
     unsigned long long timeout_ns = 2000000000ull;
     char desc[256] = "";
     mutable std::mutex mu;
@@ -285,19 +310,13 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         p->grid_tma = grid_for(p, p->tma);
     if (p->plain)
         p->grid_plain = grid_for(p, p->plain);
-    e = cudaMalloc(&p->d_err, sizeof(uint32_t));
-    if (e == cudaSuccess)
-        e = cudaMemset(p->d_err, 0, sizeof(uint32_t));
-    if (e == cudaSuccess && p->splits > 1) {
-        p->ws_rows = static_cast<int>((M + 255) / 256 * 256);
-        const size_t bytes = static_cast<size_t>(p->splits) * p->ws_rows * static_cast<size_t>(N) * sizeof(float);
-        e = cudaMalloc(&p->ws, bytes);
-        if (e == cudaSuccess && (N * 4) % 16 == 0) {
-            if (encode_2d(&p->tmW, sat::kDtTF32, p->ws, N, static_cast<uint64_t>(p->splits) * p->ws_rows, 32u, 32u,
-                          CU_TENSOR_MAP_SWIZZLE_128B) == 0)
-                p->ws_tma = true;
-        }
+    e = cudaHostAlloc(reinterpret_cast<void**>(&p->h_err), 64, cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+        *reinterpret_cast<volatile uint32_t*>(p->h_err) = 0;
+        e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->d_err), p->h_err, 0);
     }
+    if (p->splits > 1)
+        p->ws_rows = static_cast<int>((M + 255) / 256 * 256);
     // Stream-K (TMA path, unsplit): every slot runs, whatever the tile count.
     if (e == cudaSuccess && c.sk && p->tma && p->splits == 1) {
         const sat::KernelEntry* t = p->tma;
@@ -307,20 +326,14 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         const int64_t slots = slots_for(p, t);
         if (sat::sk_layout(tiles, num_kb, slots, &p->sk_tiles, &p->sk_w)) {
             p->sk_ctas = static_cast<int>(slots * t->cg);
+            p->sk_bn = t->bn;
             p->grid_tma = p->sk_ctas;
-            e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_ctas) * 128 * t->bn * sizeof(float));
-            if (e == cudaSuccess)
-                e = cudaMalloc(&p->sk_flags, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned));
-            if (e == cudaSuccess)
-                e = cudaMemset(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned));
         }
     }
     if (e != cudaSuccess) {
-        cuda_fail(e, "allocating the device error word and workspace");
-        for (void* d : {static_cast<void*>(p->d_err), static_cast<void*>(p->ws), static_cast<void*>(p->sk_ws),
-                        static_cast<void*>(p->sk_flags)})
-            if (d)
-                cudaFree(d);
+        cuda_fail(e, "allocating the host-mapped error word");
+        if (p->h_err)
+            cudaFreeHost(p->h_err);
         delete p;
         return nullptr;
     }
@@ -349,6 +362,78 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
 
 namespace {
 
+void free_scratch(Scratch& s)
+{
+    for (void* d : {static_cast<void*>(s.ws), static_cast<void*>(s.sk_ws), static_cast<void*>(s.sk_flags)})
+        if (d)
+            cudaFree(d);
+    if (s.done)
+        cudaEventDestroy(s.done);
+    s = Scratch{};
+}
+
+size_t sk_flag_bytes(const gemm_plan* p)
+{
+    return static_cast<size_t>(p->sk_ctas + kTicketPad) * sizeof(unsigned);
+}
+
+// The scratch set of `stream` (p->scratch_mu held): this stream's own, a new
+// one, or the least recently used one taken over behind its last run. A new
+// set's counters are cleared on `stream`, ahead of the run.
+int acquire_scratch(const gemm_plan* p, cudaStream_t stream, Scratch** out)
+{
+    unsigned long long id = 0;
+    cudaError_t e = cudaStreamGetId(stream, &id);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamGetId");
+    Scratch* hit = nullptr;
+    for (int i = 0; i < p->n_scratch && !hit; ++i)
+        if (p->scratch[i].stream_id == id)
+            hit = &p->scratch[i];
+    if (!hit && p->n_scratch < kMaxScratch) {
+        Scratch& s = p->scratch[p->n_scratch];
+        e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
+        if (e == cudaSuccess && p->splits > 1) {
+            const size_t bytes =
+                static_cast<size_t>(p->splits) * p->ws_rows * static_cast<size_t>(p->N) * sizeof(float);
+            e = cudaMalloc(&s.ws, bytes);
+            if (e == cudaSuccess && (p->N * 4) % 16 == 0 &&
+                encode_2d(&s.tmW, sat::kDtTF32, s.ws, p->N, static_cast<uint64_t>(p->splits) * p->ws_rows, 32u, 32u,
+                          CU_TENSOR_MAP_SWIZZLE_128B) == 0)
+                s.ws_tma = true;
+        }
+        if (e == cudaSuccess && p->sk_tiles > 0) {
+            e = cudaMalloc(&s.sk_ws, static_cast<size_t>(p->sk_ctas) * 128 * p->sk_bn * sizeof(float));
+            if (e == cudaSuccess)
+                e = cudaMalloc(&s.sk_flags, sk_flag_bytes(p));
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(s.sk_flags, 0, sk_flag_bytes(p), stream);
+        }
+        if (e != cudaSuccess) {
+            free_scratch(s);
+            return fail(e == cudaErrorMemoryAllocation ? GEMM_ERR_NOMEM : GEMM_ERR_LAUNCH,
+                        "preparing this stream's scratch: %s", cudaGetErrorString(e));
+        }
+        s.stream_id = id;
+        ++p->n_scratch;
+        hit = &s;
+    }
+    if (!hit) {
+        Scratch* v = &p->scratch[0];
+        for (int i = 1; i < p->n_scratch; ++i)
+            if (p->scratch[i].last_use < v->last_use)
+                v = &p->scratch[i];
+        e = cudaStreamWaitEvent(stream, v->done, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "ordering this stream behind the scratch's last run");
+        v->stream_id = id;
+        hit = v;
+    }
+    hit->last_use = ++p->use_clock;
+    *out = hit;
+    return GEMM_OK;
+}
+
 int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int64_t ldb, void* Cv, int64_t ldc,
              float alpha, float beta, void* cuda_stream)
 {
@@ -372,6 +457,12 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         return cuda_fail(e, "cudaGetDevice");
     if (dev != p->device)
         return fail(GEMM_ERR_ARG, "plan was made for device %d but device %d is current", p->device, dev);
+    // A kernel of this plan that gave up a bounded wait set the host-mapped
+    // error word: report it here, before enqueueing more work.
+    if (*reinterpret_cast<volatile uint32_t*>(p->h_err) != 0)
+        return fail(GEMM_ERR_TIMEOUT,
+                    "an earlier run of this plan gave up a bounded wait (its C is incomplete); nothing was enqueued; "
+                    "gemm_plan_status clears the condition");
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     if (p->K == 0 || alpha == 0.0f) {
         e = sat::launch_scale(C, p->c_half, p->M, p->N, ldc, beta, stream);
@@ -416,10 +507,21 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     a.num_tiles = a.tiles_m * a.tiles_n * a.splits;
     a.out_rows = static_cast<int>(p->M);
     const bool split = p->splits > 1;
+    const bool sk = use_tma && p->sk_tiles > 0;
+    // Split-K and stream-K runs write this stream's scratch set, held (with
+    // the plan's scratch lock) until the run is enqueued and its end recorded.
+    std::unique_lock<std::mutex> slock(p->scratch_mu, std::defer_lock);
+    Scratch* sc = nullptr;
+    if (split || sk) {
+        slock.lock();
+        const int rc = acquire_scratch(p, stream, &sc);
+        if (rc)
+            return rc;
+    }
     if (split) {
         // The GEMM writes raw fp32 partial tiles to the workspace; the
         // reduction applies alpha and beta.
-        a.C = p->ws;
+        a.C = sc->ws;
         a.ldc = static_cast<int>(p->N);
         a.c_half = 0;
         a.alpha = 1.0f;
@@ -434,32 +536,34 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     // C goes through the bulk-store epilogue when its base and row stride
     // are 16-byte multiples (a TMA store box must start on a 16-byte boundary).
     // (16-bit C always goes through the row-store epilogue.)
-    const bool c_tma = split ? p->ws_tma
+    const bool c_tma = split ? sc->ws_tma
                              : p->c_half == 0 && p->N % 4 == 0 && ldc % 4 == 0 &&
                                    reinterpret_cast<uintptr_t>(C) % 16 == 0;
     a.c_tma = c_tma ? 1 : 0;
     a.c_ring = p->c_ring && use_tma && c_tma && !split && beta != 0.0f ? 1 : 0;
-    if (use_tma && p->sk_tiles > 0) {
-        // Each launch has its own number; a slot's counter reaches number x
-        // (epilogue warps) once its partial tile of this launch is written.
-        // Before the counters could wrap, they are cleared and numbering restarts.
-        unsigned epoch = p->sk_epoch.fetch_add(1) + 1;
+    if (sk) {
+        // Each launch on a scratch set has its own number; a slot's counter
+        // reaches number x (epilogue warps) once its partial tile of this launch
+        // is written, and the ticket counter number x slots once every slot of
+        // it is handed out. Before the counters could wrap, they are cleared
+        // and numbering restarts.
+        unsigned epoch = ++sc->epoch;
         if (epoch >= (1u << 28)) {
-            e = cudaMemsetAsync(p->sk_flags, 0, static_cast<size_t>(p->sk_ctas) * sizeof(unsigned), stream);
+            e = cudaMemsetAsync(sc->sk_flags, 0, sk_flag_bytes(p), stream);
             if (e != cudaSuccess)
                 return cuda_fail(e, "clearing the stream-K counters");
-            p->sk_epoch.store(1);
-            epoch = 1;
+            sc->epoch = epoch = 1;
         }
         a.sk_tiles = p->sk_tiles;
         a.sk_w = p->sk_w;
-        a.sk_ws = p->sk_ws;
-        a.sk_flags = p->sk_flags;
+        a.sk_ws = sc->sk_ws;
+        a.sk_flags = sc->sk_flags;
+        a.sk_ticket = sc->sk_flags + p->sk_ctas + kTicketPad - 1;
         a.sk_epoch = epoch;
     }
     CUtensorMap tmA{}, tmB{}, tmC{};
     if (split && c_tma) {
-        tmC = p->tmW;
+        tmC = sc->tmW;
     } else if (c_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
         if (p->map_C != C || p->map_ldc != ldc) {
@@ -511,10 +615,15 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the GEMM kernel");
     if (split) {
-        e = sat::launch_splitk_reduce(p->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->c_half, p->M,
+        e = sat::launch_splitk_reduce(sc->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->c_half, p->M,
                                       p->N, ldc, alpha, beta, p->sm_count, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the split-K reduction");
+    }
+    if (sc) {
+        e = cudaEventRecord(sc->done, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "recording the end of the run");
     }
     return GEMM_OK;
 }
@@ -543,14 +652,10 @@ void gemm_plan_destroy(gemm_plan* plan)
 {
     if (!plan)
         return;
-    if (plan->d_err)
-        cudaFree(plan->d_err);
-    if (plan->ws)
-        cudaFree(plan->ws);
-    if (plan->sk_ws)
-        cudaFree(plan->sk_ws);
-    if (plan->sk_flags)
-        cudaFree(plan->sk_flags);
+    for (int i = 0; i < plan->n_scratch; ++i)
+        free_scratch(plan->scratch[i]);
+    if (plan->h_err)
+        cudaFreeHost(plan->h_err);
     delete plan;
 }
 
@@ -608,18 +713,18 @@ int gemm_plan_status(const gemm_plan* p)
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return cuda_fail(e, "device error");
-    uint32_t h = 0;
-    e = cudaMemcpy(&h, p->d_err, sizeof h, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess)
-        e = cudaMemset(p->d_err, 0, sizeof h);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "reading the device error word");
+    volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(p->h_err);
+    const uint32_t h = *w;
+    *w = 0;
     if (h) {
         // A launch that gave up may have left stream-K counters short of its
         // number: start the numbering again from cleared counters.
-        const size_t bytes = static_cast<size_t>(p->sk_ctas) * sizeof(unsigned);
-        if (p->sk_flags && cudaMemset(p->sk_flags, 0, bytes) == cudaSuccess)
-            p->sk_epoch.store(0);
+        std::lock_guard<std::mutex> lock(p->scratch_mu);
+        for (int i = 0; i < p->n_scratch; ++i) {
+            Scratch& s = p->scratch[i];
+            if (s.sk_flags && cudaMemset(s.sk_flags, 0, sk_flag_bytes(p)) == cudaSuccess)
+                s.epoch = 0;
+        }
         return fail(GEMM_ERR_TIMEOUT, "a bounded wait gave up inside the kernel (error bits 0x%x)", h);
     }
     return GEMM_OK;

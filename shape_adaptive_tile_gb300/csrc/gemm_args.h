@@ -42,11 +42,13 @@ struct GemmArgs {
     // in raster order are cut into k-block ranges of sk_w consecutive
     // positions of the (tile, k-block) sequence, one range per CTA slot
     // (CTA or CTA pair) g = 0 .. gridDim/cta_group - 1, taken before that
-    // slot's whole tiles sk_tiles + g, sk_tiles + g + slots, ...
+    // slot's whole tiles sk_tiles + g, sk_tiles + g + slots, ... A slot is
+    // handed out by sk_ticket in the order the slots' CTAs start.
     int sk_tiles;
     int sk_w;
     float* sk_ws;              // per slot and CTA of a pair: 128 x BN fp32 partial tile
     unsigned* sk_flags;        // per slot and CTA of a pair: epilogue warps done with the partial
+    unsigned* sk_ticket;       // slots handed out so far, over all launches on this scratch (may be null)
     unsigned sk_epoch;         // this launch's number (>= 1); a partial is ready at sk_epoch * epilogue warps
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;

@@ -39,6 +39,7 @@ constexpr uint32_t kErrTimeoutMma = 1u << 1;
 constexpr uint32_t kErrTimeoutEpilogue = 1u << 2;
 constexpr uint32_t kErrTimeoutDrain = 1u << 3;
 constexpr uint32_t kErrTimeoutPartial = 1u << 4;   // a stream-K partial tile never arrived
+constexpr uint32_t kErrTicket = 1u << 5;           // a stream-K slot ticket outside this launch's range
 
 template <int DT, int BN, int CG, int PROD>
 struct Traits {
@@ -159,13 +160,15 @@ __device__ __forceinline__ uint32_t swz_kmajor(int r, int k)
 // share that split's K slice of the operands in L2.
 //
 // Stream-K pieces come in three kinds: a whole tile; a partial piece (it
-// does not start at k-block 0), whose raw sum goes to its slot's partial
-// tile; and a final piece (k-blocks 0 .. kb1 < num_kb), which adds the
-// partial pieces of slots g + 1 .. last, in that order, before the epilogue.
+// ends before the tile's last k-block), whose raw sum goes to its slot's
+// partial tile; and a final piece (k-blocks kb0 > 0 .. num_kb), which adds
+// the partial pieces of slots first .. g - 1, in that order, before the
+// epilogue. A final piece thus waits only on slots that started before its
+// own, and only on each one's first unit.
 constexpr int kWhole = 0, kSkPartial = 1, kSkFinal = 2;
 
 struct Unit {
-    int tm, tn, s, kb0, kb1, kind, last;
+    int tm, tn, s, kb0, kb1, kind, first;
 };
 
 __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
@@ -177,14 +180,20 @@ __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
     w.kb0 = w.s * a.kb_per_split;
     w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
     w.kind = kWhole;
-    w.last = 0;
+    w.first = 0;
     return w;
 }
 
 // The sequence of units of CTA slot g out of G: its stream-K range of
-// (tile, k-block) positions [pos, end), cut at tile boundaries, then its
-// whole units t = sk_tiles + g, sk_tiles + g + G, ... Without stream-K
-// this is t = g, g + G, ...
+// (tile, k-block) positions [pos, end), cut at tile boundaries and taken
+// from the end backwards, then its whole units t = sk_tiles + g,
+// sk_tiles + g + G, ... Without stream-K this is t = g, g + G, ...
+//
+// Taken backwards, a range's first unit is the piece that starts the last
+// tile it touches (or, inside one tile, the whole range): a partial piece,
+// or a whole tile, that waits on nobody. Its last unit is the piece that
+// ends the first tile it touches, the tile's final piece, which waits for
+// the pieces of the slots before it: each is that slot's first unit.
 struct WorkIter {
     int pos, end, t;
 };
@@ -203,14 +212,16 @@ template <bool kSK = true>
 __device__ __forceinline__ bool work_next(const GemmArgs& a, int G, WorkIter& it, Unit& w)
 {
     if (kSK && it.pos < it.end) {
-        const int tile = it.pos / a.num_kb;
+        const int tile = (it.end - 1) / a.num_kb;
+        const int tstart = tile * a.num_kb;
+        const int p0 = max(it.pos, tstart);
         tile_coord(tile, a, w.tm, w.tn);
         w.s = 0;
-        w.kb0 = it.pos - tile * a.num_kb;
-        w.kb1 = min(a.num_kb, w.kb0 + (it.end - it.pos));
-        w.kind = w.kb0 > 0 ? kSkPartial : (w.kb1 < a.num_kb ? kSkFinal : kWhole);
-        w.last = (tile * a.num_kb + a.num_kb - 1) / a.sk_w;
-        it.pos += w.kb1 - w.kb0;
+        w.kb0 = p0 - tstart;
+        w.kb1 = it.end - tstart;
+        w.kind = w.kb1 < a.num_kb ? kSkPartial : (w.kb0 > 0 ? kSkFinal : kWhole);
+        w.first = tstart / a.sk_w;   // the slot whose range holds the tile's k-block 0
+        it.end = p0;
         return true;
     }
     if (it.t < a.num_tiles) {
@@ -241,8 +252,11 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
 //     of dynamic shared memory at smem_raw (the routine aligns it to 1024
 //     bytes itself), and no other use of that shared memory overlaps the call;
 //   - for CG == 2 the grid is launched in clusters of 2;
-//   - every CTA of the grid calls it (the schedule spans the whole grid), and
-//     for stream-K layouts all of the grid is resident at once;
+//   - every CTA of the grid calls it (the schedule spans the whole grid); for
+//     stream-K layouts without a ticket counter (args.sk_ticket null) the
+//     CTAs' slots follow blockIdx, so all of the grid must be resident at
+//     once (with a ticket counter, slots follow the order the CTAs start in,
+//     and no residency is assumed);
 //   - tmA, tmB, tmC are tensor maps in parameter, constant or global memory,
 //     encoded as the host entry points encode them.
 // On return the CTA's share of C is written; bulk stores are complete, and
@@ -279,7 +293,10 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     // the epilogue warps that have read their chunk of it.
     auto cfull_bar = [&](int s) { return bars + 8u * (2 * T::STAGES + 7 + s); };
     int* const c_readers = reinterpret_cast<int*>(gbars + 8 * (3 * T::STAGES + 7));
-    static_assert(8 * (3 * T::STAGES + 7) + 4 * T::STAGES <= T::BAR_BYTES, "barrier area");
+    // Stream-K: this launch's slot for the CTA (pair), from the ticket.
+    volatile uint32_t* const slot_word =
+        reinterpret_cast<volatile uint32_t*>(gbars + 8 * (3 * T::STAGES + 7) + 4 * T::STAGES);
+    static_assert(8 * (3 * T::STAGES + 7) + 4 * T::STAGES + 4 <= T::BAR_BYTES, "barrier area");
     // Shared address of 4 KB slot j of ring stage s (its A part, then its B part).
     auto ring_slot = [&](int s, int j) -> uint32_t {
         constexpr int AS = T::A_BYTES / 4096;
@@ -291,6 +308,17 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
 
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
+
+    // Stream-K slots are handed out in the order the CTAs (pairs) start: the
+    // leader's first thread takes the next ticket. A final piece waits only on
+    // slots before its own, whose CTAs have therefore started, so the fix-up
+    // needs no co-residency: it finishes when other work holds SMs, or when
+    // launches of this kind overlap on several streams (each with its own
+    // counters). The atomic's latency overlaps the barrier set-up below.
+    const bool ticketed = args.sk_tiles > 0 && args.sk_ticket != nullptr;
+    unsigned ticket = 0;
+    if (ticketed && leader && warp == 0 && lane == 0)
+        ticket = atomicAdd(args.sk_ticket, 1u);
 
     // Barrier initialisation, spread over the lanes of warp 0: lane s < STAGES
     // takes ring stage s, the next two lanes the accumulator barriers, the
@@ -318,6 +346,18 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     }
     if (args.c_tma && warp == T::EPI_WARP0 && lane == 0)
         tma_prefetch_desc(&tmC);
+    if (ticketed && leader && warp == 0 && lane == 0) {
+        // Launch sk_epoch takes tickets (sk_epoch - 1) * G .. sk_epoch * G - 1
+        // (modulo 2^32): every CTA pair of every launch takes exactly one.
+        const unsigned G = gridDim.x / CG;
+        unsigned g = ticket - (args.sk_epoch - 1u) * G;
+        if (g >= G) {   // cannot happen with one launch at a time per counter
+            if (args.err)
+                atomicOr(args.err, kErrTicket);
+            g = blockIdx.x / CG;
+        }
+        *slot_word = g;
+    }
     // Barrier initialisation is published to the CTA (and, for a pair, to
     // the peer); the producer then starts at once. Tensor memory is
     // allocated meanwhile and published only to the MMA and epilogue warps
@@ -346,7 +386,18 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     // arrives on with plain arrives (TMEM released) needs cluster scope.
     constexpr bool kClu = CG == 2;
     const int tile_step = gridDim.x / CG;
-    const int tile0 = blockIdx.x / CG;
+    // This CTA's slot: the ticket the leader took (published by the barriers
+    // above: the CTA barrier, and for a pair the cluster barrier before the
+    // peer reads the leader's word), else the launch order.
+    int tile0 = blockIdx.x / CG;
+    if (ticketed) {
+        if constexpr (CG == 2)
+            tile0 = leader ? static_cast<int>(*slot_word)
+                           : static_cast<int>(ld_shared_cluster_u32(map_to_cta(smem_u32(
+                                 const_cast<uint32_t*>(slot_word)), 0)));
+        else
+            tile0 = static_cast<int>(*slot_word);
+    }
 
     if (warp < T::NPW) {
         // ------------------------------------------------------------ producer
@@ -780,11 +831,11 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 tc_fence_after();
                 if constexpr (SK) {
                     // Stream-K final piece: the partial tiles of slots
-                    // tile0 + 1 .. w.last (same rows of the same tile) must
+                    // w.first .. tile0 - 1 (same rows of the same tile) must
                     // have been written before they are added below.
                     if (w.kind == kSkFinal) {
                         if (lane == 0) {
-                            for (int j = tile0 + 1; ok && j <= w.last; ++j)
+                            for (int j = w.first; ok && j < tile0; ++j)
                                 ok = wait_counter(args.sk_flags + j * CG + static_cast<int>(rank),
                                                   args.sk_epoch * static_cast<unsigned>(T::EPI_WARPS), wc,
                                                   kErrTimeoutPartial);
@@ -845,10 +896,10 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                                                  __uint_as_float(r[4 * q + 3]));
                                 continue;
                             }
-                            // Final piece: add the later slots' partial sums,
+                            // Final piece: add the earlier slots' partial sums,
                             // in ascending slot order.
 #pragma unroll 1
-                            for (int j = tile0 + 1; j <= w.last; ++j) {
+                            for (int j = w.first; j < tile0; ++j) {
                                 const float* slot =
                                     args.sk_ws + static_cast<int64_t>(j * CG + static_cast<int>(rank)) * (128 * BN);
 #pragma unroll

@@ -25,10 +25,12 @@
 
 namespace {
 
-// 32 MiB: 4 KiB for the status word (offset 0) and the stream-K counters
-// (offset 256, one per CTA), the rest for split-K or stream-K partial tiles.
+// 32 MiB: 4 KiB for the status word (offset 0), the stream-K slot ticket
+// (offset 128) and the stream-K counters (offset 256, one per CTA), the rest
+// for split-K or stream-K partial tiles.
 constexpr size_t kScratchBytes = size_t(32) << 20;
 constexpr size_t kStatusBytes = 4096;
+constexpr size_t kTicketOffset = 128;
 constexpr size_t kCounterOffset = 256;
 constexpr size_t kWorkspaceBytes = kScratchBytes - kStatusBytes;
 
@@ -197,8 +199,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
 
     uint32_t* status = static_cast<uint32_t*>(ds->scratch);
     float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(ds->scratch) + kStatusBytes);
-    // The array keeps the previous call's contents; the status word and the
-    // stream-K counters must start at zero (this call is launch number 1).
+    // The array keeps the previous call's contents; the status word, the
+    // stream-K ticket and counters must start at zero (this call is launch
+    // number 1).
     e = cudaMemsetAsync(status, 0, kStatusBytes, stream);
     if (e != cudaSuccess)
         return sat::fail_with(GEMM_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
@@ -245,6 +248,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
         a.sk_w = sk_w;
         a.sk_ws = ws;
         a.sk_flags = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(ds->scratch) + kCounterOffset);
+        a.sk_ticket = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(ds->scratch) + kTicketOffset);
         a.sk_epoch = 1;
     }
     if (use_tma) {

@@ -317,6 +317,59 @@ def test_plan_runs_on_two_streams():
         checks.assert_bit_exact(c.cpu().numpy(), ref32, "two streams")
 
 
+# One plan on several streams at once. Split-K and stream-K plans write
+# partial tiles and counters; each stream gets a scratch set of its own, and
+# stream-K slots follow the order their CTAs start, so runs that overlap (each
+# grid only partly resident while the others hold SMs) still finish, and
+# every output is exact.
+@pytest.mark.parametrize("dtype,M,N,K,config,tag", [
+    ("bf16", 4096, 4096, 4096, None, " sk"),             # the dispatcher's stream-K CTA-pair plan
+    ("tf32", 4096, 4096, 4096, None, " sk"),
+    ("bf16", 3000, 2000, 1024, "128,1,0,4,sk", " sk"),   # 1-SM stream-K
+    ("tf32", 128, 8192, 8192, None, " s4 "),             # the dispatcher's K split 4 ways
+])
+def test_split_plan_runs_on_overlapping_streams(dtype, M, N, K, config, tag):
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 15, "dyadic")
+    _, ref32 = oracle.gemm_full(A, B, C0, 1.5, 0.5, dtype)
+    dA, dB, dC0 = to_dev(A, dtype), to_dev(B, dtype), to_dev(C0)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = [dC0.clone() for _ in range(3 * 3)]
+    with sat.Plan(M, N, K, dtype, config) as plan:
+        desc = plan.describe()
+        assert tag in desc, desc
+        torch.cuda.synchronize()
+        for r in range(3):
+            for i, s in enumerate(streams):
+                sat.check(sat.gemm_run(plan.handle, dA, dB, outs[3 * r + i], 1.5, 0.5, s.cuda_stream))
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    for j, c in enumerate(outs):
+        checks.assert_bit_exact(c.cpu().numpy(), ref32, f"run {j} of 9 on 3 streams [{desc}]")
+
+
+def test_more_streams_than_scratch_sets():
+    # 11 streams over a plan that keeps at most 8 scratch sets: later streams
+    # take over sets behind their last runs (an event wait on the GPU).
+    for dtype, M, N, K in (("bf16", 256, 2048, 8192), ("bf16", 3000, 2000, 1024)):
+        config = None if K == 8192 else "128,1,0,4,sk"
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 16, "dyadic")
+        _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        dA, dB, dC0 = to_dev(A, dtype), to_dev(B, dtype), to_dev(C0)
+        streams = [torch.cuda.Stream() for _ in range(11)]
+        outs = [dC0.clone() for _ in range(22)]
+        with sat.Plan(M, N, K, dtype, config) as plan:
+            desc = plan.describe()
+            assert " s1 " not in desc or " sk" in desc, desc
+            torch.cuda.synchronize()
+            for r in range(2):
+                for i, s in enumerate(streams):
+                    sat.check(sat.gemm_run(plan.handle, dA, dB, outs[11 * r + i], 1.5, 0.5, s.cuda_stream))
+            torch.cuda.synchronize()
+            sat.check(plan.status())
+        for j, c in enumerate(outs):
+            checks.assert_bit_exact(c.cpu().numpy(), ref32, f"run {j} of 22 on 11 streams [{desc}]")
+
+
 # TF32 operand conversion: the pages do not say whether the tensor core
 # truncates an fp32 operand to TF32's 10 fraction bits or rounds it. Probe it
 # with values whose low fraction bits decide: each output is one product
