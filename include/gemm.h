@@ -78,6 +78,8 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
  * `config` = "bn,cg,raster,group[,splits]" (bn in {64,128,256}; cg 1 or 2,
  * where 2 needs bn >= 128; raster 0 = groups along M, 1 = along N;
  * group >= 1; splits 1..16 K splits, default 1), optionally followed by
+ * ",st<n>" (a ring of n shared-memory stages where the untransposed TMA
+ * kernel of that tile is compiled with that depth; the deepest by default),
  * ",cload" (with beta != 0 the epilogue loads C itself instead of the
  * producer fetching it through the operand ring), ",swap" (operand roles
  * exchanged: the tensor core computes C^T = B^T A^T in tiles of 128 columns
@@ -258,11 +260,14 @@ int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtyp
  * gemm_plan_create would make for this problem on a device with `sm_count`
  * SMs, given whether the TMA path is possible (`tma_ok`: K and N row
  * strides are multiples of 16 bytes). Writes
- * "bn,cg,raster,group,splits,cload,sk,swap,source" (cload: 1 if, with
- * beta != 0, the epilogue loads C itself, 0 if the producer fetches it
+ * "bn,cg,raster,group,splits,cload,sk,swap,stages,source" (cload: 1 if,
+ * with beta != 0, the epilogue loads C itself, 0 if the producer fetches it
  * through the operand ring where the kernel allows; sk: 1 for a stream-K
  * schedule of the last waves; swap: 1 if the tensor core computes C^T =
- * B^T A^T, with bn rows of C per tile; source: rule or table) into `out`
+ * B^T A^T, with bn rows of C per tile; stages: the shared-memory ring depth
+ * of the chosen kernel; source: table for an exact hit in the committed
+ * sweep table, bucket for the nearest table shape in the same power-of-two
+ * bucket of M, N and K, rule for the analytic rule) into `out`
  * (NUL-terminated, at most `out_len` bytes). Returns 0, or GEMM_ERR_ARG on
  * bad arguments.
  */

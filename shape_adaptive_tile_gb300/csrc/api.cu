@@ -224,10 +224,14 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         // Optional tags after the numbers, in any order: ",cload" (the
         // epilogue loads C itself), ",sk" (stream-K), ",plain" (plain-load
         // producer). Each is looked up first; the numbers end at the first.
-        char* tag[4] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain"),
-                        std::strstr(head, ",swap")};
+        char* tag[5] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain"),
+                        std::strstr(head, ",swap"), std::strstr(head, ",st")};
         const bool cload = tag[0] != nullptr, sk = tag[1] != nullptr, swap = tag[3] != nullptr;
         p->force_plain = tag[2] != nullptr;
+        // ",st<n>": a ring of n stages (a compiled depth of the TMA kernel).
+        int stages = 0;
+        if (tag[4] && std::sscanf(tag[4] + 3, "%d", &stages) != 1)
+            stages = -1;
         for (char* t : tag)
             if (t)
                 *t = '\0';
@@ -241,6 +245,12 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         p->choice.cload = cload ? 1 : 0;
         p->choice.sk = sk ? 1 : 0;
         p->choice.swap = swap ? 1 : 0;
+        p->choice.stages = stages;
+        if (stages < 0) {
+            fail(GEMM_ERR_ARG, "bad configuration \"%s\" (\",st\" wants a stage count)", config);
+            delete p;
+            return nullptr;
+        }
         if (swap && (p->choice.cg != 1 || p->choice.bn == 256)) {
             fail(GEMM_ERR_ARG, "bad configuration \"%s\" (a swapped tile is 1-SM with bn 32, 64 or 128)", config);
             delete p;
@@ -249,7 +259,7 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         source = "forced";
     } else {
         p->choice = sat::select_config(M, N, K, dt, sms, tma_ok);
-        source = p->choice.source == 1 ? "table" : "rule";
+        source = p->choice.source == sat::kSrcTable ? "table" : p->choice.source == sat::kSrcBucket ? "bucket" : "rule";
     }
     if (trans) {
         // Transposed layouts come as 1-SM 128 x 128 and 128 x 256 tiles and
@@ -270,9 +280,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
                          : c.swap           ? sat::kProdSwap
                                             : sat::kProdTMA;
     if (tma_ok && !p->force_plain) {
-        p->tma = sat::find_entry(dt, c.bn, c.cg, tma_kind);
+        p->tma = sat::find_entry(dt, c.bn, c.cg, tma_kind, tma_kind == sat::kProdTMA ? c.stages : 0);
         if (!p->tma) {
-            fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d in this layout", c.bn, c.cg);
+            fail(GEMM_ERR_ARG, "no compiled TMA kernel for bn=%d cg=%d stages=%d in this layout", c.bn, c.cg,
+                 c.stages);
             delete p;
             return nullptr;
         }
@@ -761,8 +772,14 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     if (M < 0 || N < 0 || K < 0 || dt < 0 || dt > 2 || sm_count < 1 || !out || out_len < 1)
         return fail(GEMM_ERR_ARG, "bad arguments to gemm_select_config");
     const sat::Choice c = sat::select_config(M, N, K, dt, sm_count, tma_ok != 0);
-    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
-                  c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.swap, c.source == 1 ? "table" : "rule");
+    // The ring depth of the kernel the choice names (the plain-load kernel's
+    // when TMA cannot read the operands).
+    const sat::KernelEntry* k = tma_ok ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA,
+                                                         c.swap ? 0 : c.stages)
+                                       : sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
+    std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
+                  c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.swap, k ? k->stages : 0,
+                  c.source == sat::kSrcTable ? "table" : c.source == sat::kSrcBucket ? "bucket" : "rule");
     return GEMM_OK;
 }
 

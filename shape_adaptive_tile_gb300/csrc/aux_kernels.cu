@@ -122,14 +122,20 @@ cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cuda
     return cudaGetLastError();
 }
 
-const KernelEntry* find_entry(int dt, int bn, int cg, int prod)
+const KernelEntry* find_entry(int dt, int bn, int cg, int prod, int stages)
 {
     const KernelEntry* tab = dt == kDtTF32 ? kEntriesTF32 : dt == kDtBF16 ? kEntriesBF16 : kEntriesFP16;
     const int n = dt == kDtTF32 ? kNumEntriesTF32 : dt == kDtBF16 ? kNumEntriesBF16 : kNumEntriesFP16;
-    for (int i = 0; i < n; ++i)
-        if (tab[i].bn == bn && tab[i].cg == cg && tab[i].prod == prod)
+    const KernelEntry* best = nullptr;
+    for (int i = 0; i < n; ++i) {
+        if (tab[i].bn != bn || tab[i].cg != cg || tab[i].prod != prod)
+            continue;
+        if (stages > 0 && tab[i].stages == stages)
             return &tab[i];
-    return nullptr;
+        if (stages == 0 && (!best || tab[i].stages > best->stages))
+            best = &tab[i];
+    }
+    return best;
 }
 
 }  // namespace sat

@@ -15,7 +15,20 @@ struct Choice {
     int cload;    // beta != 0: 1 = the epilogue loads C itself, 0 = the producer fetches it through the ring
     int sk;       // 1: stream-K for the last waves of tiles (fixed-order fix-up of split tiles)
     int swap;     // 1: operand roles exchanged (the MMA computes C^T = B^T A^T; bn tiles M), 1-SM only
+    int stages;   // shared-memory ring depth of the TMA kernel; 0: the deepest compiled for the tile
 };
+
+// Source codes of a choice.
+constexpr int kSrcRule = 0, kSrcTable = 1, kSrcForced = 2, kSrcBucket = 3;
+
+// Estimated DRAM bytes that reading the operands takes when `tiles_m` x
+// `tiles_n` output tiles (rows of `tile_rows` of A, columns of `tile_cols` of
+// B, each needing its whole K panel of `row_bytes` per row or column) run in
+// raster order (raster, group) as waves of `slots` concurrent tiles, with
+// the first `lead` tiles as one wave of their own (stream-K pieces). L2 is a
+// least-recently-used store of whole panels of `l2_bytes`.
+double operand_traffic(int64_t tiles_m, int64_t tiles_n, int64_t tile_rows, int64_t tile_cols, double row_bytes,
+                       int raster, int group, int64_t slots, int64_t lead, double l2_bytes);
 
 // Stream-K layout for T output tiles of KB k-blocks on G CTA slots: the
 // first *sk_tiles tiles (in raster order) are shared out as ranges of *sk_w

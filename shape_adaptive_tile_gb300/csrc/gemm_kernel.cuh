@@ -41,7 +41,8 @@ constexpr uint32_t kErrTimeoutDrain = 1u << 3;
 constexpr uint32_t kErrTimeoutPartial = 1u << 4;   // a stream-K partial tile never arrived
 constexpr uint32_t kErrTicket = 1u << 5;           // a stream-K slot ticket outside this launch's range
 
-template <int DT, int BN, int CG, int PROD>
+// ST: shared-memory ring depth, 0 for the most stages that fit.
+template <int DT, int BN, int CG, int PROD, int ST = 0>
 struct Traits {
     static constexpr bool PLAIN = PROD == kProdPlain || PROD == kProdPlainStrided;  // plain-load producer warps
     static constexpr bool TMA = !PLAIN;  // one elected thread issues TMA loads
@@ -82,7 +83,8 @@ struct Traits {
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int BUDGET = 227 * 1024 - 1024 - EPI_BYTES - BAR_BYTES;
-    static constexpr int STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
+    static constexpr int MAX_STAGES = (BUDGET / STAGE_BYTES) > 8 ? 8 : (BUDGET / STAGE_BYTES);
+    static constexpr int STAGES = ST > 0 && ST < MAX_STAGES ? ST : MAX_STAGES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int NPW = TMA ? 1 : 4;   // producer warps
     static constexpr int MMA_WARP = NPW;
@@ -262,11 +264,11 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
 // On return the CTA's share of C is written; bulk stores are complete, and
 // the CTA's tensor memory is freed. The routine's own work is all inside
 // the call: nothing is left pending for the caller.
-template <int DT, int BN, int CG, int PROD>
+template <int DT, int BN, int CG, int PROD, int ST = 0>
 __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                          const GemmArgs& args, uint8_t* smem_raw)
 {
-    using T = Traits<DT, BN, CG, PROD>;
+    using T = Traits<DT, BN, CG, PROD, ST>;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1102,13 +1104,13 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     }
 }
 
-template <int DT, int BN, int CG, int PROD>
-__global__ void __launch_bounds__(Traits<DT, BN, CG, PROD>::THREADS, 1)
+template <int DT, int BN, int CG, int PROD, int ST>
+__global__ void __launch_bounds__(Traits<DT, BN, CG, PROD, ST>::THREADS, 1)
     sat_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
-    gemm_cta<DT, BN, CG, PROD>(tmA, tmB, tmC, args, smem_raw);
+    gemm_cta<DT, BN, CG, PROD, ST>(tmA, tmB, tmC, args, smem_raw);
 }
 
 }  // namespace sat

@@ -6,19 +6,19 @@
 
 namespace sat {
 
-template <int DT, int BN, int CG, int PROD>
+template <int DT, int BN, int CG, int PROD, int ST>
 cudaError_t prepare_variant()
 {
-    using T = Traits<DT, BN, CG, PROD>;
-    return cudaFuncSetAttribute(sat_gemm_kernel<DT, BN, CG, PROD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    using T = Traits<DT, BN, CG, PROD, ST>;
+    return cudaFuncSetAttribute(sat_gemm_kernel<DT, BN, CG, PROD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 T::SMEM_BYTES);
 }
 
-template <int DT, int BN, int CG, int PROD>
+template <int DT, int BN, int CG, int PROD, int ST>
 cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const CUtensorMap* tmC,
                            const GemmArgs* args, int grid, cudaStream_t stream)
 {
-    using T = Traits<DT, BN, CG, PROD>;
+    using T = Traits<DT, BN, CG, PROD, ST>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(T::THREADS, 1, 1);
@@ -33,13 +33,13 @@ cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD>, *tmA, *tmB, *tmC, *args);
+    return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD, ST>, *tmA, *tmB, *tmC, *args);
 }
 
-template <int DT, int BN, int CG, int PROD>
+template <int DT, int BN, int CG, int PROD, int ST>
 int max_clusters_variant()
 {
-    using T = Traits<DT, BN, CG, PROD>;
+    using T = Traits<DT, BN, CG, PROD, ST>;
     if (CG != 2)
         return 0;
     int dev = 0, sms = 0;
@@ -58,17 +58,17 @@ int max_clusters_variant()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sat_gemm_kernel<DT, BN, CG, PROD>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, sat_gemm_kernel<DT, BN, CG, PROD, ST>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-template <int DT, int BN, int CG, int PROD>
+template <int DT, int BN, int CG, int PROD, int ST>
 constexpr KernelEntry make_entry()
 {
-    using T = Traits<DT, BN, CG, PROD>;
+    using T = Traits<DT, BN, CG, PROD, ST>;
     return KernelEntry{DT,
                        BN,
                        CG,
@@ -82,19 +82,27 @@ constexpr KernelEntry make_entry()
                        T::C_RING_OK ? 1 : 0,
                        T::A_MN ? 1 : 0,
                        T::B_KM ? 1 : 0,
-                       &prepare_variant<DT, BN, CG, PROD>, &max_clusters_variant<DT, BN, CG, PROD>,
-                       &launch_variant<DT, BN, CG, PROD>};
+                       &prepare_variant<DT, BN, CG, PROD, ST>, &max_clusters_variant<DT, BN, CG, PROD, ST>,
+                       &launch_variant<DT, BN, CG, PROD, ST>};
 }
 
 // The variants compiled for every dtype.
+// The untransposed TMA tiles come with two ring depths each: the most
+// stages that fit, and a shallower ring (a dispatcher dimension, measured by
+// the sweep).
 #define SAT_ENTRIES(DT)                                                                                         \
-    make_entry<DT, 64, 1, kProdTMA>(), make_entry<DT, 128, 1, kProdTMA>(), make_entry<DT, 256, 1, kProdTMA>(), \
-        make_entry<DT, 128, 2, kProdTMA>(), make_entry<DT, 256, 2, kProdTMA>(),                                 \
-        make_entry<DT, 128, 1, kProdPlain>(), make_entry<DT, 256, 1, kProdPlain>(),                             \
-        make_entry<DT, 128, 1, kProdPlainStrided>(), make_entry<DT, 256, 1, kProdPlainStrided>(),               \
-        make_entry<DT, 32, 1, kProdSwap>(), make_entry<DT, 64, 1, kProdSwap>(), make_entry<DT, 128, 1, kProdSwap>(), \
-        make_entry<DT, 128, 1, kProdTN>(), make_entry<DT, 256, 1, kProdTN>(), make_entry<DT, 256, 2, kProdTN>(),    \
-        make_entry<DT, 128, 1, kProdNT>(), make_entry<DT, 256, 1, kProdNT>(), make_entry<DT, 256, 2, kProdNT>(),    \
-        make_entry<DT, 128, 1, kProdTT>(), make_entry<DT, 256, 1, kProdTT>(), make_entry<DT, 256, 2, kProdTT>()
+    make_entry<DT, 64, 1, kProdTMA, 0>(), make_entry<DT, 128, 1, kProdTMA, 0>(),                                \
+        make_entry<DT, 256, 1, kProdTMA, 0>(), make_entry<DT, 128, 2, kProdTMA, 0>(),                           \
+        make_entry<DT, 256, 2, kProdTMA, 0>(), make_entry<DT, 64, 1, kProdTMA, 4>(),                            \
+        make_entry<DT, 128, 1, kProdTMA, 4>(), make_entry<DT, 256, 1, kProdTMA, 3>(),                           \
+        make_entry<DT, 128, 2, kProdTMA, 4>(), make_entry<DT, 256, 2, kProdTMA, 4>(),                           \
+        make_entry<DT, 128, 1, kProdPlain, 0>(), make_entry<DT, 256, 1, kProdPlain, 0>(),                       \
+        make_entry<DT, 128, 1, kProdPlainStrided, 0>(), make_entry<DT, 256, 1, kProdPlainStrided, 0>(),         \
+        make_entry<DT, 32, 1, kProdSwap, 0>(), make_entry<DT, 64, 1, kProdSwap, 0>(),                           \
+        make_entry<DT, 128, 1, kProdSwap, 0>(), make_entry<DT, 128, 1, kProdTN, 0>(),                           \
+        make_entry<DT, 256, 1, kProdTN, 0>(), make_entry<DT, 256, 2, kProdTN, 0>(),                             \
+        make_entry<DT, 128, 1, kProdNT, 0>(), make_entry<DT, 256, 1, kProdNT, 0>(),                             \
+        make_entry<DT, 256, 2, kProdNT, 0>(), make_entry<DT, 128, 1, kProdTT, 0>(),                             \
+        make_entry<DT, 256, 1, kProdTT, 0>(), make_entry<DT, 256, 2, kProdTT, 0>()
 
 }  // namespace sat

@@ -151,7 +151,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     const bool tma_ok = (K * es) % 16 == 0 && (N * es) % 16 == 0;
     const sat::Choice c = sat::select_config(M, N, K, dt, ds->sm_count, tma_ok);
     const bool use_tma = tma_ok && reinterpret_cast<uintptr_t>(A) % 16 == 0 && reinterpret_cast<uintptr_t>(B) % 16 == 0;
-    const sat::KernelEntry* k = use_tma ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA)
+    const sat::KernelEntry* k = use_tma ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA,
+                                                          c.swap ? 0 : c.stages)
                                         : sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
     if (!k)
         return sat::fail_with(GEMM_ERR_ARG, "no compiled kernel for the chosen configuration");

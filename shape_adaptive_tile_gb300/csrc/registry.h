@@ -50,8 +50,9 @@ int fail_with(int code, const char* fmt, ...);
 int encode_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const void* ptr, uint64_t inner,
                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
-// Finds the variant, or nullptr.
-const KernelEntry* find_entry(int dt, int bn, int cg, int prod);
+// Finds the variant with `stages` ring stages (0: the deepest ring compiled
+// for that tile), or nullptr.
+const KernelEntry* find_entry(int dt, int bn, int cg, int prod, int stages = 0);
 
 // The output tiles of a variant, as rows of tiles (the accumulator's 128 x
 // cta_group rows) and columns of tiles (its bn columns). A swapped variant

@@ -71,6 +71,20 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
     return out
 
 
+# Shallower ring depths compiled for the untransposed TMA tiles, by (bn, cg).
+ALT_STAGES = {(64, 1): 4, (128, 1): 4, (256, 1): 3, (128, 2): 4, (256, 2): 4}
+
+
+def stage_variants(config):
+    """The configuration with each other compiled ring depth (",st<n>"), for
+    untransposed TMA tiles; none for plain-load or swapped ones."""
+    parts = config.split(",")
+    if "plain" in parts or "swap" in parts:
+        return []
+    alt = ALT_STAGES.get((int(parts[0]), int(parts[1])))
+    return [f"{config},st{alt}"] if alt else []
+
+
 def time_config(sat, torch, M, N, K, dtype, config, dA, dB, dC, flush, runs, warmup, alpha=1.0, beta=0.0):
     stream = torch.cuda.current_stream()
     with sat.Plan(M, N, K, dtype, config) as plan:
@@ -99,10 +113,20 @@ def sweep_shape(sat, torch, M, N, K, dtype, runs=30, warmup=3, configs=None, alp
     dC = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to("cuda")
     flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
     res = []
-    for cfg in configs or candidates(M, N, K, dtype, tma_ok, beta=beta):
+
+    def run(cfg):
         r = time_config(sat, torch, M, N, K, dtype, cfg, dA, dB, dC, flush, runs, warmup, alpha, beta)
         r["tflops"] = 2.0 * M * N * K / (r["median_ms"] * 1e-3) / 1e12
         res.append(r)
+
+    for cfg in configs or candidates(M, N, K, dtype, tma_ok, beta=beta):
+        run(cfg)
+    # Ring depth, the last dimension: the three fastest configurations again
+    # with each shallower compiled ring.
+    if tma_ok and not configs:
+        for best in sorted(res, key=lambda r: r["median_ms"])[:3]:
+            for cfg in stage_variants(best["config"]):
+                run(cfg)
     with sat.Plan(M, N, K, dtype) as p:
         chosen = p.describe()
     return {"dtype": dtype, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta, "results": res,
@@ -119,8 +143,9 @@ def table_row(e):
     cload = 1 if "cload" in parts[4:] else 0
     sk = 1 if "sk" in parts[4:] else 0
     swap = 1 if "swap" in parts[4:] else 0
+    stages = next((int(p[2:]) for p in parts[4:] if p.startswith("st") and p[2:].isdigit()), 0)
     return (f"{{{DT_CODE[e['dtype']]}, {e['M']}, {e['N']}, {e['K']}, {{{bn}, {cg}, {raster}, {group}, 0, {splits}, "
-            f"{cload}, {sk}, {swap}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
+            f"{cload}, {sk}, {swap}, {stages}}}}},  // {best['tflops']:.1f} TFLOP/s, {best['median_ms'] * 1e3:.1f} us")
 
 
 def _key(line):
@@ -140,7 +165,7 @@ def write_table(entries, path=TABLE, merge=False):
                     rows[k] = line.rstrip("\n")
     for e in entries:
         rows[(DT_CODE[e["dtype"]], e["M"], e["N"], e["K"])] = table_row(e)
-    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload, sk, swap}}.",
+    lines = ["// Committed sweep table: {dtype, M, N, K, {bn, cg, raster, group, 0, splits, cload, sk, swap, stages}}.",
              "// Written by shape_adaptive_tile_gb300/sweep.py from on-device timings",
              "// (median of L2-flushed runs) of every candidate configuration."]
     order = {1: 0, 2: 1, 0: 2}  # bf16, fp16, tf32

@@ -57,7 +57,8 @@ def test_plan_create_fails_cleanly_without_a_gpu(lib):
 
 
 def _choice(M, N, K, dt, sms=152, tma=True):
-    bn, cg, raster, group, splits, cload, sk, swap, source = sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
+    bn, cg, raster, group, splits, cload, sk, swap, stages, source = \
+        sat.gemm_select_config(M, N, K, dt, sms, tma).split(",")
     return int(bn), int(cg), int(raster), int(group), int(splits), source
 
 
@@ -189,3 +190,50 @@ def test_noalloc_scratch_holds_every_dispatcher_choice_on_a_gb300():
                     worst = max(worst, need)
                     assert need <= limit, (dt, M, N, K, f, need)
     assert 0 < worst <= sms * 128 * 256 * 4
+
+
+def _fields(M, N, K, dt, tma=True):
+    return sat.gemm_select_config(M, N, K, dt, 152, tma).split(",")
+
+
+def test_dispatcher_reports_the_ring_depth():
+    # The chosen kernel's shared-memory ring: 6 stages for the CTA-pair
+    # 256-wide tile, 4 for the 1-SM 256-wide tile, 8 for 1-SM 64-wide ones.
+    f = _fields(8192, 8192, 8192, "tf32")
+    assert f[:2] == ["256", "2"] and f[8] == "6" and f[9] == "table"
+    f = _fields(768, 768, 768, "tf32")
+    assert f[0] == "64" and f[8] == "8"
+    for M, N, K in [(5000, 5000, 5000), (333, 517, 389), (1, 4096, 4096)]:
+        for dt in ("tf32", "bf16"):
+            assert int(_fields(M, N, K, dt)[8]) >= 2
+
+
+def test_dispatcher_bucket_serves_shapes_next_to_the_table():
+    # One row or one k off a swept shape: the same power-of-two bucket, the
+    # swept shape's choice.
+    for M, N, K, dt, near in [(8192, 8192, 8191, "bf16", (8192, 8192, 8192)),
+                              (8000, 8100, 8192, "tf32", (8192, 8192, 8192)),
+                              (4095, 4096, 4096, "bf16", (4096, 4096, 4096)),
+                              (16000, 1000, 4000, "tf32", (16384, 1024, 4096)),
+                              (120, 8192, 8000, "bf16", (128, 8192, 8192))]:
+        f, g = _fields(M, N, K, dt), _fields(*near, dt)
+        assert f[9] == "bucket" and g[9] == "table", (M, N, K, f, g)
+        assert f[:9] == g[:9], (M, N, K, f, g)
+    # Outside every bucket: the rule.
+    assert _fields(1500, 1500, 1500, "bf16")[9] == "rule"
+    # The misaligned (8191, 4097, 2049) row serves plain-load shapes only.
+    assert _fields(8190, 4099, 2051, "tf32", tma=False)[9] == "bucket"
+    assert _fields(8192, 8192, 4096, "tf32")[9] != "bucket" or _fields(8192, 8192, 4096, "tf32")[1] == "2"
+
+
+def test_rule_picks_the_raster_group_with_least_modelled_traffic():
+    # No table row near either shape, 76 CTA pairs. bf16 12288^3: a wave of
+    # 76 tiles spans ~17 operand panels of 6 MB at best (groups of 8 or 16
+    # tile-rows), more than L2 keeps between waves, so the group must keep a
+    # wave square; groups of 1 would touch ~50 panels per wave.
+    f = _fields(12288, 12288, 12288, "bf16")
+    assert f[9] == "rule" and f[1] == "2" and int(f[3]) >= 8
+    # bf16 6144 x 6144 x 4096: B's 24 column panels (48 MB) fit in L2, so
+    # waves running along whole tile-rows (group 1) read A and B once.
+    f = _fields(6144, 6144, 4096, "bf16")
+    assert f[9] == "rule" and f[2:4] == ["0", "1"]

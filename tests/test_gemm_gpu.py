@@ -30,7 +30,10 @@ CONFIGS = ["256,1,0,8", "128,1,0,8", "64,1,1,4", "256,2,0,4", "128,2,1,2", "256,
            "256,1,0,8,plain", "128,1,1,3,plain",
            "256,1,0,8,3", "128,2,0,4,2", "64,1,1,2,4", "128,1,0,2,3,plain",
            "256,2,0,4,sk", "128,1,0,8,sk", "64,1,1,4,sk",
-           "128,1,0,4,swap", "64,1,1,2,swap", "32,1,0,8,swap", "64,1,0,2,3,swap"]
+           "128,1,0,4,swap", "64,1,1,2,swap", "32,1,0,8,swap", "64,1,0,2,3,swap",
+           # the shallower compiled rings (a dispatcher dimension)
+           "256,2,0,4,st4", "128,2,1,2,st4", "256,1,0,8,st3", "128,1,0,8,st4", "64,1,1,4,st4",
+           "256,2,0,4,sk,st4", "128,1,0,8,cload,st4", "128,2,0,4,2,st4"]
 SHAPES = [(333, 517, 389), (129, 65, 33), (1, 1, 1), (7, 300, 5), (256, 256, 256), (513, 100, 130)]
 
 
@@ -315,6 +318,29 @@ def test_plan_runs_on_two_streams():
         torch.cuda.synchronize()
     for c in outs:
         checks.assert_bit_exact(c.cpu().numpy(), ref32, "two streams")
+
+
+# Shapes next to a swept one take its choice through the power-of-two bucket
+# (M, N and K rounding up to the same powers of two); every output exact.
+@pytest.mark.parametrize("dtype,M,N,K", [("bf16", 8000, 8104, 8192), ("tf32", 4000, 4000, 4000),
+                                         ("bf16", 120, 8192, 8000)])
+def test_bucket_chosen_plan_dyadic_exact(dtype, M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")[-1] == "bucket"
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 17, "dyadic")
+    _, ref32 = oracle.gemm_full(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5)
+    assert " bucket" in desc, desc
+    checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+def test_forced_ring_depth_is_the_compiled_one():
+    with sat.Plan(512, 512, 512, "bf16", "256,2,0,4,st4") as p:
+        assert " st4 " in p.describe()
+    with sat.Plan(512, 512, 512, "bf16", "256,2,0,4") as p:
+        assert " st6 " in p.describe()
+    with pytest.raises(sat.GemmError):
+        sat.Plan(512, 512, 512, "bf16", "256,2,0,4,st5")
 
 
 # One plan on several streams at once. Split-K and stream-K plans write

@@ -80,7 +80,7 @@ def test_noalloc_matches_gemm_run_on_two_calls(case):
 
 def _split_workspace_bytes(M, N, K, dtype):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    bn, cg, _, _, splits, _, _, swap, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
+    bn, cg, _, _, splits, _, _, swap, _, _ = sat.gemm_select_config(M, N, K, dtype, sms, True).split(",")
     rows = 128 * int(cg)
     return int(splits), int(splits) * (-(-M // rows) * rows) * N * 4
 
