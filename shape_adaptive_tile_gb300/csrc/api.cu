@@ -91,6 +91,7 @@ struct Scratch {
     float* sk_ws = nullptr;            // stream-K: one 128 x bn float partial tile per CTA
     unsigned* sk_flags = nullptr;      // stream-K: one counter per CTA, then the ticket counter
     unsigned epoch = 0;                // stream-K launches on these counters since they were cleared
+    void* bpack = nullptr;             // B with 16-byte-aligned rows (K x ldb_pack elements), when B's are not
     cudaEvent_t done = nullptr;        // recorded after each run that used this set
     unsigned long long last_use = 0;
 };
@@ -112,6 +113,11 @@ struct gemm_plan {
     const sat::KernelEntry* tma = nullptr;    // null when the strides rule out TMA
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
     const sat::KernelEntry* plain_strided = nullptr;  // the same, for row strides other than K and N
+    // Class-view kernel for operand rows that TMA cannot address directly
+    // (untransposed plans): A through one tensor map per residue class of row
+    // index, B aligned or packed into the stream's scratch (ldb_pack).
+    const sat::KernelEntry* cls = nullptr;
+    int64_t slots_cls = 0, ldb_pack = 0;
     int grid_tma = 0, grid_plain = 0;
     // Error word in host-mapped pinned memory: kernels OR bits into it through
     // d_err; the host reads h_err without synchronising.
@@ -135,6 +141,15 @@ struct gemm_plan {
     mutable const void* map_C = nullptr;
     mutable int64_t map_lda = 0, map_ldb = 0, map_ldc = 0;
     mutable CUtensorMap tmA{}, tmB{}, tmC{};
+    // Class views of A (for the A pointer and stride they were made for).
+    mutable const void* cls_A = nullptr;
+    mutable int64_t cls_lda = 0;
+    mutable int cls_n = 0;
+    mutable int cls_shift[sat::kMaxClasses] = {}, cls_rows[sat::kMaxClasses] = {};
+    mutable CUtensorMap tmCls[sat::kMaxClasses];
+    mutable const void* cls_B = nullptr;
+    mutable int64_t cls_ldb = 0;
+    mutable CUtensorMap tmClsB{};
 };
 
 namespace {
@@ -297,7 +312,17 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             return nullptr;
         }
     }
-    for (const sat::KernelEntry* k : {p->tma, p->plain, p->plain_strided}) {
+    if (!trans && !p->force_plain) {
+        // The class-view kernel serves operand rows that TMA cannot address:
+        // the choice's tile where one is compiled (1-SM 128 or 256 columns,
+        // CTA-pair 256).
+        const int bn = c.cg == 2 ? 256 : (c.bn < 128 ? 128 : c.bn);
+        p->cls = sat::find_entry(dt, bn, c.cg, sat::kProdClassA);
+        if (p->cls)
+            p->slots_cls = slots_for(p, p->cls);
+        p->ldb_pack = (N * es + 15) / 16 * 16 / es;
+    }
+    for (const sat::KernelEntry* k : {p->tma, p->plain, p->plain_strided, p->cls}) {
         if (!k)
             continue;
         e = k->prepare();
@@ -353,14 +378,15 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         if (ms > 0)
             p->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
-    const sat::KernelEntry* k = p->tma ? p->tma : p->plain;
+    const sat::KernelEntry* k = p->tma ? p->tma : p->cls ? p->cls : p->plain;
     p->c_ring = !c.cload && p->tma && p->tma->c_ring && p->splits == 1 && p->sk_tiles == 0 && p->c_half == 0;
     char sk_desc[48] = "";
     if (p->sk_tiles)
         std::snprintf(sk_desc, sizeof sk_desc, " sk%d/%d", p->sk_tiles, p->sk_w);
     std::snprintf(p->desc, sizeof p->desc, "%s m%lld n%lld k%lld: bn%d cg%d st%d %s raster%d g%d s%d grid%d %s%s%s%s%s%s",
                   dt_name(dt), (long long)M, (long long)N, (long long)K, k->bn, k->cg, k->stages,
-                  p->tma ? "tma" : "plain", c.raster, c.group, p->splits, p->tma ? p->grid_tma : p->grid_plain,
+                  p->tma ? "tma" : p->cls ? "cls" : "plain", c.raster, c.group, p->splits,
+                  p->tma ? p->grid_tma : p->cls ? static_cast<int>(p->slots_cls * p->cls->cg) : p->grid_plain,
                   source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "",
                   trans_a ? " ta" : "", trans_b ? " tb" : "");
     if (c_type)
@@ -375,7 +401,7 @@ namespace {
 
 void free_scratch(Scratch& s)
 {
-    for (void* d : {static_cast<void*>(s.ws), static_cast<void*>(s.sk_ws), static_cast<void*>(s.sk_flags)})
+    for (void* d : {static_cast<void*>(s.ws), static_cast<void*>(s.sk_ws), static_cast<void*>(s.sk_flags), s.bpack})
         if (d)
             cudaFree(d);
     if (s.done)
@@ -391,7 +417,7 @@ size_t sk_flag_bytes(const gemm_plan* p)
 // The scratch set of `stream` (p->scratch_mu held): this stream's own, a new
 // one, or the least recently used one taken over behind its last run. A new
 // set's counters are cleared on `stream`, ahead of the run.
-int acquire_scratch(const gemm_plan* p, cudaStream_t stream, Scratch** out)
+int acquire_scratch(const gemm_plan* p, cudaStream_t stream, bool want_pack, Scratch** out)
 {
     unsigned long long id = 0;
     cudaError_t e = cudaStreamGetId(stream, &id);
@@ -440,6 +466,15 @@ int acquire_scratch(const gemm_plan* p, cudaStream_t stream, Scratch** out)
         v->stream_id = id;
         hit = v;
     }
+    if (want_pack && !hit->bpack) {
+        const size_t bytes = static_cast<size_t>(p->K) * static_cast<size_t>(p->ldb_pack) * elem_size(p->dt);
+        e = cudaMalloc(&hit->bpack, bytes);
+        if (e != cudaSuccess) {
+            hit->bpack = nullptr;
+            return fail(e == cudaErrorMemoryAllocation ? GEMM_ERR_NOMEM : GEMM_ERR_LAUNCH,
+                        "allocating this stream's aligned copy of B: %s", cudaGetErrorString(e));
+        }
+    }
     hit->last_use = ++p->use_clock;
     *out = hit;
     return GEMM_OK;
@@ -485,15 +520,20 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     if (reinterpret_cast<uintptr_t>(A) % es || reinterpret_cast<uintptr_t>(B) % es)
         return fail(GEMM_ERR_ALIGN, "A and B must be aligned to their %d-byte element size", (int)es);
     // TMA needs 16-byte aligned bases and row strides.
-    const bool use_tma = p->tma && reinterpret_cast<uintptr_t>(A) % 16 == 0 &&
-                         reinterpret_cast<uintptr_t>(B) % 16 == 0 && (lda * static_cast<int64_t>(es)) % 16 == 0 &&
-                         (ldb * static_cast<int64_t>(es)) % 16 == 0;
-    if (!use_tma && !p->plain)
+    const int64_t es64 = static_cast<int64_t>(es);
+    const bool a_rows_ok = reinterpret_cast<uintptr_t>(A) % 16 == 0 && (lda * es64) % 16 == 0;
+    const bool b_rows_ok = reinterpret_cast<uintptr_t>(B) % 16 == 0 && (ldb * es64) % 16 == 0;
+    const bool use_tma = p->tma && a_rows_ok && b_rows_ok;
+    // Otherwise (untransposed plans) the class-view kernel: A through one
+    // tensor map per residue class of row index, B as it lies when its rows
+    // are aligned, else packed into this stream's aligned copy.
+    const bool use_cls = !use_tma && p->cls != nullptr;
+    if (!use_tma && !use_cls && !p->plain)
         return fail(GEMM_ERR_ALIGN,
                     "transposed operands are read by TMA only: A and B must be 16-byte aligned with row strides "
                     "that are multiples of 16 bytes");
     const bool dense = lda == p->K && ldb == p->N;
-    const sat::KernelEntry* k = use_tma ? p->tma : dense ? p->plain : p->plain_strided;
+    const sat::KernelEntry* k = use_tma ? p->tma : use_cls ? p->cls : dense ? p->plain : p->plain_strided;
 
     sat::GemmArgs a{};
     a.M = static_cast<int>(p->M);
@@ -510,22 +550,87 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     a.beta = beta;
     int64_t tiles_m = 0, tiles_n = 0;
     sat::tile_grid(k, p->M, p->N, &tiles_m, &tiles_n);
+    a.num_kb = static_cast<int>((p->K + k->bk - 1) / k->bk);
+    int splits = p->splits, kbps = p->kb_per_split;
+    if (use_cls) {
+        // Residue classes of A's rows: row m starts (A + m * lda * es) mod 16
+        // bytes past a 16-byte boundary, which repeats with period P. Class r
+        // (rows r + P*y) is read from a view starting that many bytes earlier,
+        // so every class's view rows are 16-byte aligned. Output tiles take
+        // 128 x cta_group view rows of one class; K runs over the views'
+        // extra leading elements too.
+        std::lock_guard<std::mutex> lock(p->mu);
+        if (p->cls_A != A || p->cls_lda != lda) {
+            const int64_t rb = lda * es64;
+            int g = static_cast<int>(rb % 16);
+            int P = 16;
+            while (g && P > 1 && g % 2 == 0 && P % 2 == 0) {
+                g /= 2;
+                P /= 2;
+            }
+            if (g == 0)
+                P = 1;
+            const CUtensorMapDataType t = p->dt == sat::kDtTF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                          : p->dt == sat::kDtBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+            for (int r = 0; r < P; ++r) {
+                const uintptr_t start = reinterpret_cast<uintptr_t>(A) + static_cast<uintptr_t>(r * rb);
+                const int delta = static_cast<int>(start % 16);
+                const int64_t rows = r < p->M ? (p->M - r + P - 1) / P : 0;
+                p->cls_shift[r] = delta / static_cast<int>(es);
+                p->cls_rows[r] = static_cast<int>(rows);
+                // A class without rows reads class 0's view (its tiles store nothing).
+                const int src = rows > 0 ? r : 0;
+                const uintptr_t sstart = reinterpret_cast<uintptr_t>(A) + static_cast<uintptr_t>(src * rb);
+                const int sdelta = static_cast<int>(sstart % 16);
+                const int64_t srows = (p->M - src + P - 1) / P;
+                const int rc = sat::encode_map(&p->tmCls[r], t, static_cast<int>(es),
+                                               reinterpret_cast<const void*>(sstart - sdelta),
+                                               static_cast<uint64_t>(p->K + sdelta / static_cast<int>(es)),
+                                               static_cast<uint64_t>(srows), static_cast<uint64_t>(P * lda),
+                                               static_cast<uint32_t>(k->bk), 128u, CU_TENSOR_MAP_SWIZZLE_128B);
+                if (rc) {
+                    p->cls_A = nullptr;
+                    return fail(GEMM_ERR_LAUNCH, "cuTensorMapEncodeTiled failed for a class view of A (%d)", rc);
+                }
+            }
+            p->cls_n = P;
+            p->cls_A = A;
+            p->cls_lda = lda;
+        }
+        a.a_classes = p->cls_n;
+        int smax = 0;
+        for (int r = 0; r < p->cls_n; ++r) {
+            a.a_shift[r] = p->cls_shift[r];
+            a.a_rows[r] = p->cls_rows[r];
+            smax = std::max(smax, p->cls_shift[r]);
+        }
+        const int64_t per_class = (p->M + p->cls_n - 1) / p->cls_n;
+        tiles_m = p->cls_n * ((per_class + 128 * k->cg - 1) / (128 * k->cg));
+        a.num_kb = static_cast<int>((p->K + smax + k->bk - 1) / k->bk);
+        if (splits > 1) {
+            // The same slices of the workspace, over the views' k-blocks.
+            kbps = (a.num_kb + splits - 1) / splits;
+            splits = (a.num_kb + kbps - 1) / kbps;
+        }
+    }
     a.tiles_m = static_cast<int>(tiles_m);
     a.tiles_n = static_cast<int>(tiles_n);
-    a.num_kb = static_cast<int>((p->K + k->bk - 1) / k->bk);
-    a.splits = p->splits;
-    a.kb_per_split = p->splits > 1 ? p->kb_per_split : a.num_kb;
+    a.splits = splits;
+    a.kb_per_split = splits > 1 ? kbps : a.num_kb;
     a.num_tiles = a.tiles_m * a.tiles_n * a.splits;
     a.out_rows = static_cast<int>(p->M);
-    const bool split = p->splits > 1;
+    const bool split = splits > 1;
     const bool sk = use_tma && p->sk_tiles > 0;
-    // Split-K and stream-K runs write this stream's scratch set, held (with
-    // the plan's scratch lock) until the run is enqueued and its end recorded.
+    const bool pack = use_cls && !b_rows_ok;
+    // Split-K and stream-K runs, and class-view runs whose B must be packed,
+    // write this stream's scratch set, held (with the plan's scratch lock)
+    // until the run is enqueued and its end recorded.
     std::unique_lock<std::mutex> slock(p->scratch_mu, std::defer_lock);
     Scratch* sc = nullptr;
-    if (split || sk) {
+    if (split || sk || pack) {
         slock.lock();
-        const int rc = acquire_scratch(p, stream, &sc);
+        const int rc = acquire_scratch(p, stream, pack, &sc);
         if (rc)
             return rc;
     }
@@ -589,6 +694,34 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         }
         tmC = p->tmC;
     }
+    if (use_cls) {
+        // B as it lies, or packed into rows of ldb_pack elements (16-byte
+        // multiples) first, on the same stream.
+        const void* bsrc = B;
+        int64_t bld = ldb;
+        if (pack) {
+            e = sat::launch_pack_rows(B, ldb * es64, sc->bpack, p->ldb_pack * es64, p->K, p->N * es64, p->sm_count,
+                                      stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "launching the packing of B");
+            bsrc = sc->bpack;
+            bld = p->ldb_pack;
+        }
+        std::lock_guard<std::mutex> lock(p->mu);
+        if (p->cls_B != bsrc || p->cls_ldb != bld) {
+            const int rc = encode_2d(&p->tmClsB, p->dt, bsrc, p->N, p->K, static_cast<uint32_t>(128 / es),
+                                     static_cast<uint32_t>(k->bk), static_cast<CUtensorMapSwizzle>(k->b_swizzle), bld);
+            if (rc) {
+                p->cls_B = nullptr;
+                return rc;
+            }
+            p->cls_B = bsrc;
+            p->cls_ldb = bld;
+        }
+        tmB = p->tmClsB;
+        a.c_tma = 0;
+        a.c_ring = 0;
+    }
     if (use_tma) {
         std::lock_guard<std::mutex> lock(p->mu);
         // Each operand as it lies: K contiguous (boxes of BK x rows, 128-byte
@@ -622,11 +755,24 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         tmA = p->tmA;
         tmB = p->tmB;
     }
-    e = k->launch(&tmA, &tmB, &tmC, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
+    if (use_cls) {
+        // Class maps are copied under the lock: another thread may re-encode them.
+        CUtensorMap cmaps[sat::kMaxClasses];
+        {
+            std::lock_guard<std::mutex> lock(p->mu);
+            for (int r = 0; r < a.a_classes; ++r)
+                cmaps[r] = p->tmCls[r];
+        }
+        const int64_t units = static_cast<int64_t>(a.num_tiles);
+        const int grid = static_cast<int>((units < p->slots_cls ? units : p->slots_cls) * k->cg);
+        e = k->launch(cmaps, &tmB, &tmC, &a, grid, stream);
+    } else {
+        e = k->launch(&tmA, &tmB, &tmC, &a, use_tma ? p->grid_tma : p->grid_plain, stream);
+    }
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the GEMM kernel");
     if (split) {
-        e = sat::launch_splitk_reduce(sc->ws, p->splits, static_cast<long long>(p->ws_rows) * p->N, C, p->c_half, p->M,
+        e = sat::launch_splitk_reduce(sc->ws, splits, static_cast<long long>(p->ws_rows) * p->N, C, p->c_half, p->M,
                                       p->N, ldc, alpha, beta, p->sm_count, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "launching the split-K reduction");
@@ -776,7 +922,8 @@ int gemm_select_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, int 
     // when TMA cannot read the operands).
     const sat::KernelEntry* k = tma_ok ? sat::find_entry(dt, c.bn, c.cg, c.swap ? sat::kProdSwap : sat::kProdTMA,
                                                          c.swap ? 0 : c.stages)
-                                       : sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
+                                       : sat::find_entry(dt, c.cg == 2 ? 256 : (c.bn < 128 ? 128 : c.bn), c.cg,
+                                                         sat::kProdClassA);
     std::snprintf(out, static_cast<size_t>(out_len), "%d,%d,%d,%d,%d,%d,%d,%d,%d,%s", c.bn, c.cg, c.raster, c.group,
                   c.splits > 1 ? c.splits : 1, c.cload, c.sk, c.swap, k ? k->stages : 0,
                   c.source == sat::kSrcTable ? "table" : c.source == sat::kSrcBucket ? "bucket" : "rule");

@@ -1,5 +1,6 @@
-// Small kernels around the GEMM: C = beta * C for K == 0 or alpha == 0, the
-// registry lookup, and the bounded-wait self-test.
+// Small kernels around the GEMM: C = beta * C for K == 0 or alpha == 0, row
+// packing of operands whose rows are not 16-byte aligned, the split-K
+// reduction, the registry lookup, and the bounded-wait self-test.
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -25,6 +26,67 @@ cudaError_t launch_scale(float* C, int kind, long long rows, long long cols, lon
         return cudaSuccess;
     const long long blocks = rows < 8192 ? rows : 8192;
     sat_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, kind, rows, cols, ldc, beta);
+    return cudaGetLastError();
+}
+
+// Row packing for operands whose rows are not 16-byte aligned: dst row r is
+// src row r (cols elements of `es` bytes, row stride ld_src), written with
+// row stride ld_dst (a multiple of 16 bytes, dst 16-byte aligned) and zeros
+// after the last column. Each thread writes one 16-byte piece of dst, read
+// from src as aligned-down 4-byte words (elements are es-aligned, so a piece
+// spans at most five words) shifted into place: copying order only, no
+// arithmetic on the values. Memory-bound: one read and one write per element.
+__global__ void sat_pack_rows_kernel(const uint8_t* __restrict__ src, long long ld_src_bytes, uint8_t* __restrict__ dst,
+                                     long long ld_dst_bytes, long long rows, long long row_bytes)
+{
+    const long long pieces = ld_dst_bytes / 16;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * pieces; i += stride) {
+        const long long r = i / pieces, b0 = (i - r * pieces) * 16;  // byte offset of the piece within the row
+        const uint8_t* row = src + r * ld_src_bytes;
+        uint32_t out[4];
+        if (b0 + 16 <= row_bytes) {
+            // Whole piece inside the row: five aligned words cover it.
+            const uintptr_t a = reinterpret_cast<uintptr_t>(row + b0);
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+            const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+            uint32_t v[5];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[j] = __ldg(w + j);
+            v[4] = sh ? __ldg(w + 4) : 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                out[j] = sh ? __funnelshift_r(v[j], v[j + 1], sh) : v[j];
+        } else {
+            // The row's last piece: bytes past the row are zero.
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t word = 0;
+                for (int b = 0; b < 4; ++b) {
+                    const long long o = b0 + 4 * j + b;
+                    if (o < row_bytes)
+                        word |= static_cast<uint32_t>(__ldg(row + o)) << (8 * b);
+                }
+                out[j] = word;
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + r * ld_dst_bytes + b0) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+cudaError_t launch_pack_rows(const void* src, long long ld_src_bytes, void* dst, long long ld_dst_bytes,
+                             long long rows, long long row_bytes, int sm_count, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    const long long work = rows * (ld_dst_bytes / 16);
+    long long blocks = (work + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    sat_pack_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), ld_src_bytes, static_cast<uint8_t*>(dst), ld_dst_bytes, rows, row_bytes);
     return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(ProbeTraits<DT>::THREADS, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     // Phase 1: this CTA's share of the GEMM.
-    sat::gemm_cta<DT, 128, 1, sat::kProdTMA>(tmA, tmB, tmC, args, smem_raw);
+    sat::gemm_cta<DT, 128, 1, sat::kProdTMA>(&tmA, tmB, tmC, args, smem_raw);
     // Phase 2: ReLU over the same tiles, in the order the schedule gave them.
     __syncthreads();
     sat::WorkIter it = sat::work_begin(args, blockIdx.x);

@@ -191,13 +191,17 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
         if (!tma_ok && c.bn <= 64)
             c.bn = 128;
         if (!tma_ok) {
+            // class-view tiles: 1-SM 128 or 256 columns, CTA-pair 256
             c.swap = 0;
             c.stages = 0;
+            c.sk = 0;
+            if (c.cg == 2)
+                c.bn = 256;
         }
         return c;
     };
     for (const TableRow& r : kTable)
-        if (r.dt == dt && r.M == M && r.N == N && r.K == K && (tma_ok || r.c.cg == 1))
+        if (r.dt == dt && r.M == M && r.N == N && r.K == K)
             return from_row(r, kSrcTable);
     // Power-of-two buckets: the nearest swept shape (in log2 distance) whose
     // M, N and K round up to the same powers of two and that took the same
@@ -222,16 +226,20 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     }
     // Analytic rule, calibrated on the sweep: per-SM dense tensor rate
     // (bf16/fp16 8192 FLOP per clock, tf32 4096), a sustained operand fill
-    // from L2 of about 64 bytes per clock per SM for TMA (the plain-load path
-    // fills far slower), about 22 bytes per clock of HBM bandwidth per SM
-    // (6.7 TB/s over 152 SMs at ~2 GHz), and a fixed cost per wave
-    // (prologue, pipeline fill, final epilogue).
+    // from L2 of about 64 bytes per clock per SM for TMA, about 22 bytes per
+    // clock of HBM bandwidth per SM (6.7 TB/s over 152 SMs at ~2 GHz), and a
+    // fixed cost per wave (prologue, pipeline fill, final epilogue). Rows that
+    // TMA cannot address directly (tma_ok false) take the class-view kernels,
+    // also TMA-fed: 1-SM 128 or 256 columns, or CTA-pair 256; B is first
+    // packed into aligned rows when its own are not (one read and one write
+    // of B more).
     const double es = dt == 0 ? 4.0 : 2.0;
     const double flop_clk = dt == 0 ? 4096.0 : 8192.0;
-    const double fill_clk = tma_ok ? 64.0 : 12.0;
+    const double fill_clk = 64.0;
     const double hbm_clk = 22.0 * sm_count;
     const double wave_cost = 6000.0;
-    const double hbm = (es * (double)(M * K + K * N) + 8.0 * (double)(M * N)) / hbm_clk;
+    const double pack = !tma_ok && (N * static_cast<int64_t>(es)) % 16 != 0 ? 2.0 * es * (double)(K * N) / hbm_clk : 0.0;
+    const double hbm = (es * (double)(M * K + K * N) + 8.0 * (double)(M * N)) / hbm_clk + pack;
     struct Cand { int bn, cg, swap; };
     // Tiles of a candidate: 128 x cta_group rows by bn columns of C, or,
     // swapped, 128 columns by bn rows.
@@ -242,7 +250,7 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     double best_t = 1e300;
     Choice best{256, 1, 0, 8, 0};
     for (const Cand& cd : cands) {
-        if (!tma_ok && (cd.cg == 2 || cd.bn == 64 || cd.swap))
+        if (!tma_ok && (cd.bn == 64 || cd.swap || (cd.cg == 2 && cd.bn != 256)))
             continue;
         if (cd.cg == 2 && M <= 128)
             continue;  // a CTA pair would leave its second 128 rows empty
@@ -252,7 +260,7 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
         // Per CTA: its MMA share and the bytes it loads per unit of K.
         const double mma = 2.0 * 128.0 * cd.bn * K / flop_clk;
         const double fill = (128.0 + cd.bn / cd.cg) * es * K / fill_clk;
-        const double t = std::max(waves * (std::max(mma, fill) + wave_cost), hbm);
+        const double t = std::max(waves * (std::max(mma, fill) + wave_cost) + pack, hbm);
         // Prefer the larger tile unless the smaller is clearly faster.
         if (t < best_t * 0.97) {
             best_t = t;

@@ -18,6 +18,13 @@ constexpr int kProdTN = 3;     // TMA loads, A stored transposed (K x M): first 
 constexpr int kProdNT = 4;     // TMA loads, B stored transposed (N x K): second operand K-major
 constexpr int kProdTT = 5;     // TMA loads, both stored transposed
 constexpr int kProdPlainStrided = 6;  // plain loads with row strides lda, ldb other than K, N
+// TMA loads for rows that are not 16-byte aligned: A's rows are read through
+// one tensor map per residue class of row index (rows m = r + P*y, whose
+// byte offsets share one misalignment, aligned down), each output tile
+// taking rows of one class; B is read from rows aligned in memory (the
+// caller's, or an aligned copy), shifted in K by the class's offset.
+constexpr int kProdClassA = 7;
+constexpr int kMaxClasses = 8;
 
 struct GemmArgs {
     int M, N, K;
@@ -50,6 +57,13 @@ struct GemmArgs {
     unsigned* sk_flags;        // per slot and CTA of a pair: epilogue warps done with the partial
     unsigned* sk_ticket;       // slots handed out so far, over all launches on this scratch (may be null)
     unsigned sk_epoch;         // this launch's number (>= 1); a partial is ready at sk_epoch * epilogue warps
+    // Class-view A (kProdClassA): P = a_classes residue classes of rows; class
+    // r holds rows r + P*y, y < a_rows[r], read from a view that starts
+    // a_shift[r] elements before each row (the aligned-down start). Output
+    // tile rows tm = r + P*j: class r, view rows from j*128*cta_group.
+    int a_classes;
+    int a_rows[kMaxClasses];
+    int a_shift[kMaxClasses];
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;
 };

@@ -53,6 +53,11 @@ struct Traits {
     // contiguous, K-major). For skinny M, where 128-row tiles of C would be
     // mostly empty.
     static constexpr bool SWAP = PROD == kProdSwap;
+    // Class-view A (rows whose byte offsets are not 16-byte aligned): one
+    // tensor map per residue class of row index, and a fixer warp that zeroes
+    // the elements of the previous row that each tile's first k-block reads
+    // in front of every row (the views start aligned down).
+    static constexpr bool CLS = PROD == kProdClassA;
     // Operand layouts in shared memory: the first MMA operand (the
     // accumulator's rows) MN-major when it comes from a matrix stored with
     // those rows contiguous (A stored K x M, or B for a swapped tile), else
@@ -89,7 +94,8 @@ struct Traits {
     static constexpr int NPW = TMA ? 1 : 4;   // producer warps
     static constexpr int MMA_WARP = NPW;
     static constexpr int EPI_WARP0 = NPW + 1;
-    static constexpr int THREADS = (NPW + 1 + EPI_WARPS) * 32;
+    static constexpr int FIX_WARP = CLS ? EPI_WARP0 + EPI_WARPS : -1;
+    static constexpr int THREADS = (NPW + 1 + EPI_WARPS + (CLS ? 1 : 0)) * 32;
     static constexpr int ACC_COLS = BN;             // fp32 accumulator: one column per element
     // beta != 0: the producer can fetch each tile's C (this CTA's BM x BN
     // fp32 block, as 32 x 32 chunks of 4 KB in the 128-byte swizzle) through
@@ -260,12 +266,13 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
 //     once (with a ticket counter, slots follow the order the CTAs start in,
 //     and no residency is assumed);
 //   - tmA, tmB, tmC are tensor maps in parameter, constant or global memory,
-//     encoded as the host entry points encode them.
+//     encoded as the host entry points encode them (tmA points to one map,
+//     or for class-view A to one map per residue class).
 // On return the CTA's share of C is written; bulk stores are complete, and
 // the CTA's tensor memory is freed. The routine's own work is all inside
 // the call: nothing is left pending for the caller.
 template <int DT, int BN, int CG, int PROD, int ST = 0>
-__device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+__device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                          const GemmArgs& args, uint8_t* smem_raw)
 {
     using T = Traits<DT, BN, CG, PROD, ST>;
@@ -298,14 +305,21 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     // Stream-K: this launch's slot for the CTA (pair), from the ticket.
     volatile uint32_t* const slot_word =
         reinterpret_cast<volatile uint32_t*>(gbars + 8 * (3 * T::STAGES + 7) + 4 * T::STAGES);
-    static_assert(8 * (3 * T::STAGES + 7) + 4 * T::STAGES + 4 <= T::BAR_BYTES, "barrier area");
+    // Class-view A: per stage, the barrier a tile's first k-block of A lands
+    // on when the fixer warp must zero its leading elements first.
+    constexpr uint32_t kAfix = (8u * (3 * T::STAGES + 8) + 4u * T::STAGES + 7u) & ~7u;  // 8-byte aligned
+    auto afix_bar = [&](int s) { return bars + kAfix + 8u * s; };
+    static_assert(kAfix + 8 * T::STAGES <= T::BAR_BYTES, "barrier area");
     // Shared address of 4 KB slot j of ring stage s (its A part, then its B part).
     auto ring_slot = [&](int s, int j) -> uint32_t {
         constexpr int AS = T::A_BYTES / 4096;
         return j < AS ? sA + static_cast<uint32_t>(s * T::A_BYTES + j * 4096)
                       : sB + static_cast<uint32_t>(s * T::B_BYTES + (j - AS) * 4096);
     };
-    const bool c_ring = T::C_RING_OK && args.c_ring != 0 && args.c_tma != 0 && args.splits == 1 && args.sk_tiles == 0 &&
+    // Class-view tiles hold rows P apart: their C goes out by rows, never as
+    // bulk-store boxes.
+    const int c_tma = T::CLS ? 0 : args.c_tma;
+    const bool c_ring = T::C_RING_OK && args.c_ring != 0 && c_tma != 0 && args.splits == 1 && args.sk_tiles == 0 &&
                         args.beta != 0.0f;
 
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
@@ -331,6 +345,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
             mbar_init(full_bar(lane), T::TMA ? 1 : T::NPW * 32);
             mbar_init(empty_bar(lane), 1);
             mbar_init(cfull_bar(lane), 1);
+            if constexpr (T::CLS)
+                mbar_init(afix_bar(lane), 1);
             c_readers[lane] = 0;
         } else if (lane < T::STAGES + 2) {
             mbar_init(tfull_bar(lane - T::STAGES), 1);
@@ -343,10 +359,11 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
         fence_mbar_init();
     }
     if (T::TMA && warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
+        for (int i = 0; i < (T::CLS ? args.a_classes : 1); ++i)
+            tma_prefetch_desc(tmA + i);
         tma_prefetch_desc(&tmB);
     }
-    if (args.c_tma && warp == T::EPI_WARP0 && lane == 0)
+    if (c_tma && warp == T::EPI_WARP0 && lane == 0)
         tma_prefetch_desc(&tmC);
     if (ticketed && leader && warp == 0 && lane == 0) {
         // Launch sk_epoch takes tickets (sk_epoch - 1) * G .. sk_epoch * G - 1
@@ -369,7 +386,9 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     if constexpr (CG == 2)
         cluster_sync();
     uint32_t tmem_base = 0;
-    if (warp >= T::MMA_WARP) {
+    // The MMA warp and the epilogue warps (not the fixer warp of class-view
+    // kernels): exactly the (1 + EPI_WARPS) warps named barrier 1 counts.
+    if (warp >= T::MMA_WARP && warp < T::EPI_WARP0 + T::EPI_WARPS) {
         if (warp == T::MMA_WARP) {
             tmem_alloc<CG>(smem_u32(tmem_slot), T::TMEM_COLS);
             tmem_relinquish<CG>();
@@ -414,7 +433,13 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 WorkIter it = work_begin(args, tile0);
                 Unit w;
                 while (ok && work_next(args, tile_step, it, w)) {
-                    const int m0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM;
+                    // Class-view A: the tile's rows are view rows of class
+                    // cls (rows cls + P*y), whose view starts ashift elements
+                    // before each row; B follows that shift in K.
+                    const int cls = T::CLS ? w.tm % args.a_classes : 0;
+                    const int ashift = T::CLS ? args.a_shift[cls] : 0;
+                    const int tmv = T::CLS ? w.tm / args.a_classes : w.tm;
+                    const int m0 = tmv * (T::BM * CG) + static_cast<int>(rank) * T::BM;
                     const int n0 = w.tn * BN + static_cast<int>(rank) * T::BN_CTA;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
@@ -428,8 +453,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                         // each as it lies in memory: K-major as one box of
                         // BK x rows, MN-major as boxes of CW rows x BK. A
                         // swapped tile reads the first from B, the second from A.
-                        const CUtensorMap* t1 = T::SWAP ? &tmB : &tmA;
-                        const CUtensorMap* t2 = T::SWAP ? &tmA : &tmB;
+                        const CUtensorMap* t1 = T::SWAP ? &tmB : tmA + cls;
+                        const CUtensorMap* t2 = T::SWAP ? tmA : &tmB;
                         auto load = [&](uint32_t dst, const CUtensorMap* t, int x, int y) {
                             if constexpr (CG == 1)
                                 tma_load_2d(dst, t, fb, x, y);
@@ -447,15 +472,28 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
 #pragma unroll
                             for (int j = 0; j < T::NBOX_A; ++j)
                                 load(sA + stage * T::A_BYTES + j * (T::BK * 128), t1, m0 + j * T::CW, k0);
+                        } else if constexpr (T::CLS) {
+                            // A tile's first k-block reads ashift elements of the
+                            // previous row in front of each row: it lands on this
+                            // CTA's fix barrier, and the fixer warp zeroes them and
+                            // completes the bytes on the full barrier.
+                            if (kb == 0 && ashift > 0) {
+                                mbar_arrive_expect_tx(afix_bar(stage), T::A_BYTES);
+                                tma_load_2d(sA + stage * T::A_BYTES, t1, afix_bar(stage), k0, m0);
+                            } else {
+                                load(sA + stage * T::A_BYTES, t1, k0, m0);
+                            }
                         } else {
                             load(sA + stage * T::A_BYTES, t1, k0, m0);
                         }
                         if constexpr (T::B_KM) {
                             load(sB + stage * T::B_BYTES, t2, k0, n0);
                         } else {
+                            // Class-view A: K positions k0 - ashift .. of B (rows
+                            // above 0 read as zero).
 #pragma unroll
                             for (int j = 0; j < T::NBOX; ++j)
-                                load(sB + stage * T::B_BYTES + j * (T::BK * 128), t2, n0 + j * T::CW, k0);
+                                load(sB + stage * T::B_BYTES + j * (T::BK * 128), t2, n0 + j * T::CW, k0 - ashift);
                         }
                         if (++stage == T::STAGES) {
                             stage = 0;
@@ -702,8 +740,15 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * T::ACC_COLS);
+                // Class-view A in a pair: a tile's first k-block may be completed
+                // by the peer's fixer (plain stores, then a cluster-scope fence
+                // and complete_tx), so that wait acquires at cluster scope.
+                const bool fix0 = T::CLS && CG == 2 && w.kb0 == 0 && args.a_shift[w.tm % args.a_classes] > 0;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bar<false>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma)) {
+                    const bool got = fix0 && kb == 0
+                                         ? wait_bar<kClu>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma)
+                                         : wait_bar<false>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma);
+                    if (!got) {
                         ok = false;
                         break;
                     }
@@ -762,6 +807,45 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 }
             }
         }
+    } else if (T::CLS && warp == T::FIX_WARP) {
+        // --------------------------------------------------------------- fixer
+        // Class-view A: a tile's first k-block reads, in front of each row, the
+        // ashift elements of memory that precede it (the view starts aligned
+        // down). Once that block has landed, zero those elements of all 128
+        // rows (K-major, 128-byte swizzle), make the stores visible to the
+        // tensor core and complete the block's bytes on the full barrier (the
+        // pair leader's), which the producer left open for them.
+        if constexpr (T::CLS) {
+            int stage = 0;
+            uint32_t apar = 0;  // per stage: parity of its next fix
+            const uint32_t full0 = CG == 2 ? map_to_cta(full_bar(0), 0) : full_bar(0);
+            WorkIter it = work_begin(args, tile0);
+            Unit w;
+            while (work_next(args, tile_step, it, w)) {
+                const int ashift = args.a_shift[w.tm % args.a_classes];
+                if (w.kb0 == 0 && ashift > 0) {
+                    if (!wait_bar<false>(afix_bar(stage), (apar >> stage) & 1u, wc, kErrTimeoutProducer))
+                        break;
+                    apar ^= 1u << stage;
+                    const uint32_t a0 = sA + stage * T::A_BYTES;
+                    for (int i = lane; i < T::BM * ashift; i += 32) {
+                        const int row = i / ashift, k = i - row * ashift;
+                        if constexpr (T::ES == 4)
+                            st_shared_u32(a0 + swz_kmajor<4>(row, k), 0u);
+                        else
+                            st_shared_u16(a0 + swz_kmajor<2>(row, k), static_cast<uint16_t>(0));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_cluster();
+                        mbar_complete_tx_cluster(full0 + 8u * stage, T::A_BYTES);
+                    }
+                    __syncwarp();
+                }
+                stage = (stage + (w.kb1 - w.kb0)) % T::STAGES;
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - T::EPI_WARP0;      // 0..7
@@ -804,8 +888,12 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
             // ahead (the first one before the accumulator wait); the
             // stream-K copy reads it only when the chunk is stored, after any
             // partial sums have been added, to keep its registers in bounds.
-            const bool prefetch_c = MODE == 0 && !T::SWAP && args.c_tma && beta != 0.0f;
-            const bool late_c = SK && !T::SWAP && args.c_tma && beta != 0.0f;
+            const bool prefetch_c = MODE == 0 && !T::SWAP && c_tma && beta != 0.0f;
+            const bool late_c = SK && !T::SWAP && c_tma && beta != 0.0f;
+            // Row-store path (C not 16-byte aligned), beta != 0: each chunk's
+            // 32 rows of C at this lane's column are loaded together, all in
+            // flight at once.
+            const bool rows_c = MODE == 0 && !T::SWAP && !c_tma && beta != 0.0f;
             // C through the ring: where the next unit's stages start, and per
             // stage the parity of its next C fill.
             int rpos = 0;
@@ -814,8 +902,17 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
             // The stream-K copy takes this CTA's stream-K pieces; the others
             // take whole units (all of them, or those after the pieces).
             while (ok && (SK ? it.pos < it.end : true) && work_next<SK>(args, tile_step, it, w)) {
-                const int row0 = w.tm * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
+                // Class-view tiles: view rows of class cls, actual rows
+                // cls + P * (view row).
+                const int ncls = T::CLS ? args.a_classes : 1;
+                const int cls = T::CLS ? w.tm % ncls : 0;
+                const int row0 = (T::CLS ? w.tm / ncls : w.tm) * (T::BM * CG) + static_cast<int>(rank) * T::BM + sub * 32;
                 const int n0 = w.tn * BN;
+                // Row-store addressing of this warp's 32 rows: the first one's
+                // element offset (before the column), the step between rows
+                // and how many lie inside C. Split s writes its slice of the
+                // output: rows s * out_rows + row.
+                const int yoff = w.s * args.out_rows;
                 int cst = 0;  // ring stage holding this tile's first C chunks
                 if constexpr (RING) {
                     cst = (rpos + (w.kb1 - w.kb0)) % T::STAGES;
@@ -847,8 +944,6 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                             break;
                     }
                 }
-                // Split s writes its slice of the output: rows s * out_rows + row.
-                const int yoff = w.s * args.out_rows;
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) +
                                        static_cast<uint32_t>(acc * T::ACC_COLS);
                 if constexpr (NCHUNK < CSTEP) {
@@ -927,7 +1022,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                             ct[j] = beta != 0.0f && crow + j < args.M && ccol < args.N
                                         ? c_load(args.C, args.c_half, static_cast<int64_t>(crow + j) * ldc + ccol)
                                         : 0.0f;
-                        if (args.c_tma) {
+                        if (c_tma) {
                             // Stage the 32 x 32 block of C (rows crow.., columns
                             // row0..) in the store's 128-byte swizzle: row j, piece
                             // lane / 4 at (lane / 4) ^ (j & 7); conflict free.
@@ -964,7 +1059,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                         }
                         continue;
                     }
-                    if (args.c_tma) {
+                    if (c_tma) {
                         // Bulk-store path: this thread owns row (row0 + lane) of the
                         // 32 x 32 chunk. Stage it in the store's 128-byte swizzle
                         // (16-byte piece q of row l at position q ^ (l & 7): each
@@ -1035,21 +1130,39 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                     // buffer (element (row l, column j) at l*32 + (j ^ l): conflict
                     // free both ways), then each row is written by the warp as 32
                     // consecutive floats, masked to M x N.
+                    const int col = gcol0 + lane;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         buf[lane * 32 + (j ^ lane)] = __uint_as_float(r[j]);
+                    // This warp's 32 rows: the first one's element offset at
+                    // this column, the step between rows, how many lie in C.
+                    // Split s writes its slice of the output (rows s * out_rows
+                    // + row); class-view rows are cls + P * (view row).
+                    const int64_t c0 =
+                        (static_cast<int64_t>(yoff) + (T::CLS ? cls + ncls * row0 : row0)) * ldc + col;
+                    const int64_t rstep = T::CLS ? static_cast<int64_t>(ncls) * ldc : static_cast<int64_t>(ldc);
+                    const int nrows = T::CLS ? min(32, args.a_rows[cls] - row0) : min(32, args.M - row0);
+                    // beta != 0: the chunk's C at this column, all 32 loads in
+                    // flight at once (the accumulator values now sit in the
+                    // buffer, which frees their registers).
+                    if constexpr (!RING) {
+                        if (rows_c) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                cv[i] = i < nrows && col < args.N ? c_load(args.C, args.c_half, c0 + i * rstep) : 0.0f;
+                        }
+                    }
                     __syncwarp();
-                    const int col = gcol0 + lane;
                     if (col < args.N) {
-                        const int64_t c0 = (static_cast<int64_t>(yoff) + row0) * ldc + col;
-                        const int rows = min(32, args.M - row0);
                         const int kind = args.c_half;
-#pragma unroll 4
-                        for (int i = 0; i < rows; ++i) {
-                            float v = alpha * buf[i * 32 + (lane ^ i)];
-                            if (beta != 0.0f)
-                                v = fmaf(beta, c_load(args.C, kind, c0 + static_cast<int64_t>(i) * ldc), v);
-                            c_store(args.C, kind, c0 + static_cast<int64_t>(i) * ldc, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (i < nrows) {
+                                float v = alpha * buf[i * 32 + (lane ^ i)];
+                                if (beta != 0.0f)
+                                    v = fmaf(beta, rows_c ? cv[i] : c_load(args.C, kind, c0 + i * rstep), v);
+                                c_store(args.C, kind, c0 + i * rstep, v);
+                            }
                         }
                     }
                     __syncwarp();
@@ -1086,7 +1199,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
         } else {
             tile_loop(Plain{});
         }
-        if (args.c_tma && lane == 0) {
+        if (c_tma && lane == 0) {
             bulk_wait<0>();  // every bulk store of this warp has completed
             fence_proxy_async_global();
         }
@@ -1110,7 +1223,21 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD, ST>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
-    gemm_cta<DT, BN, CG, PROD, ST>(tmA, tmB, tmC, args, smem_raw);
+    gemm_cta<DT, BN, CG, PROD, ST>(&tmA, tmB, tmC, args, smem_raw);
+}
+
+// One A tensor map per residue class of row index (class-view A).
+struct ClassMaps {
+    CUtensorMap a[kMaxClasses];
+};
+
+template <int DT, int BN, int CG, int ST>
+__global__ void __launch_bounds__(Traits<DT, BN, CG, kProdClassA, ST>::THREADS, 1)
+    sat_gemm_cls_kernel(const __grid_constant__ ClassMaps tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    gemm_cta<DT, BN, CG, kProdClassA, ST>(tmA.a, tmB, tmC, args, smem_raw);
 }
 
 }  // namespace sat

@@ -6,11 +6,21 @@
 
 namespace sat {
 
+// The kernel of a variant: class-view A takes one tensor map per class.
+template <int DT, int BN, int CG, int PROD, int ST>
+constexpr auto kernel_of()
+{
+    if constexpr (PROD == kProdClassA)
+        return sat_gemm_cls_kernel<DT, BN, CG, ST>;
+    else
+        return sat_gemm_kernel<DT, BN, CG, PROD, ST>;
+}
+
 template <int DT, int BN, int CG, int PROD, int ST>
 cudaError_t prepare_variant()
 {
     using T = Traits<DT, BN, CG, PROD, ST>;
-    return cudaFuncSetAttribute(sat_gemm_kernel<DT, BN, CG, PROD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(kernel_of<DT, BN, CG, PROD, ST>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 T::SMEM_BYTES);
 }
 
@@ -33,7 +43,15 @@ cudaError_t launch_variant(const CUtensorMap* tmA, const CUtensorMap* tmB, const
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD, ST>, *tmA, *tmB, *tmC, *args);
+    if constexpr (PROD == kProdClassA) {
+        // tmA points to args->a_classes maps, one per residue class of row index.
+        ClassMaps maps{};
+        for (int i = 0; i < args->a_classes && i < kMaxClasses; ++i)
+            maps.a[i] = tmA[i];
+        return cudaLaunchKernelEx(&cfg, sat_gemm_cls_kernel<DT, BN, CG, ST>, maps, *tmB, *tmC, *args);
+    } else {
+        return cudaLaunchKernelEx(&cfg, sat_gemm_kernel<DT, BN, CG, PROD, ST>, *tmA, *tmB, *tmC, *args);
+    }
 }
 
 template <int DT, int BN, int CG, int PROD, int ST>
@@ -58,7 +76,7 @@ int max_clusters_variant()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sat_gemm_kernel<DT, BN, CG, PROD, ST>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_of<DT, BN, CG, PROD, ST>(), &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -103,6 +121,8 @@ constexpr KernelEntry make_entry()
         make_entry<DT, 256, 1, kProdTN, 0>(), make_entry<DT, 256, 2, kProdTN, 0>(),                             \
         make_entry<DT, 128, 1, kProdNT, 0>(), make_entry<DT, 256, 1, kProdNT, 0>(),                             \
         make_entry<DT, 256, 2, kProdNT, 0>(), make_entry<DT, 128, 1, kProdTT, 0>(),                             \
-        make_entry<DT, 256, 1, kProdTT, 0>(), make_entry<DT, 256, 2, kProdTT, 0>()
+        make_entry<DT, 256, 1, kProdTT, 0>(), make_entry<DT, 256, 2, kProdTT, 0>(),                             \
+        make_entry<DT, 128, 1, kProdClassA, 0>(), make_entry<DT, 256, 1, kProdClassA, 0>(),                     \
+        make_entry<DT, 256, 2, kProdClassA, 0>()
 
 }  // namespace sat

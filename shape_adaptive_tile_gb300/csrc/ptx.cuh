@@ -46,6 +46,28 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Completes `bytes` of the transaction count of an mbarrier (this CTA's, or
+// the pair leader's through a shared::cluster address) without a copy: for
+// operand bytes that threads wrote into shared memory themselves. Relaxed:
+// order the writes first (proxy fence, then fence_acq_rel_cluster).
+__device__ __forceinline__ void mbar_complete_tx_cluster(uint32_t bar_cluster, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(bar_cluster), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // 32-bit load from a shared::cluster address (this CTA's or a peer's).
 __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr)
 {

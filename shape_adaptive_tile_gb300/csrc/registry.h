@@ -69,6 +69,8 @@ inline void tile_grid(const KernelEntry* e, int64_t M, int64_t N, int64_t* tiles
 cudaError_t launch_scale(float* C, int kind, long long rows, long long cols, long long ldc, float beta,
                          cudaStream_t stream);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cudaStream_t stream);
+cudaError_t launch_pack_rows(const void* src, long long ld_src_bytes, void* dst, long long ld_dst_bytes,
+                             long long rows, long long row_bytes, int sm_count, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* ws, int S, long long slice, float* C, int kind, long long rows,
                                  long long cols, long long ldc, float alpha, float beta, int sm_count,
                                  cudaStream_t stream);

@@ -35,7 +35,9 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
     out = []
     kb = -(-K // (32 if dtype == "tf32" else 64))
     for bn, cg in ((256, 2), (128, 2), (256, 1), (128, 1), (64, 1)):
-        if not tma_ok and (cg == 2 or bn == 64):
+        # Rows TMA cannot address directly take the class-view tiles (1-SM
+        # 128 or 256 columns, CTA-pair 256), compared with the plain loads.
+        if not tma_ok and (bn == 64 or (cg == 2 and bn != 256)):
             continue
         if cg == 2 and M <= 128:
             continue
@@ -51,6 +53,9 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
             # tile has no ring stages to spare, so it always loads C itself)
             if beta != 0.0 and tma_ok and (bn, cg) != (256, 1):
                 out.append(f"{bn},{cg},{raster},{group},cload")
+        if not tma_ok and cg == 1:
+            for raster, group in itertools.product((0, 1), (2, 4)):
+                out.append(f"{bn},{cg},{raster},{group},plain")
         # K splits only where the tiles alone leave at least half the SMs idle
         ctas = -(-M // (128 * cg)) * -(-N // bn) * cg
         for s in (2, 4, 8):

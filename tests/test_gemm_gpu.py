@@ -224,24 +224,66 @@ def test_empty_m_or_n_is_a_no_op():
             torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("which", ["A", "B", "AB"])
+@pytest.mark.parametrize("config", [None, "256,2,0,4", "128,1,1,2", "256,1,0,8,plain"])
 @pytest.mark.parametrize("dtype", ["tf32", "bf16"])
-def test_misaligned_pointers_take_the_plain_path(dtype):
+def test_misaligned_pointers(dtype, config, which):
     """Operands that start one element past a 16-byte boundary cannot be
-    described by a TMA tensor map; the plan switches to the plain-load
-    producer and must give the same bits."""
-    M, N, K = 150, 264, 96      # row strides 16-byte multiples: TMA-able when aligned
+    described by a TMA tensor map as they lie. A goes through its class view
+    (here one class, every row shifted by one element); B, whose rows are then
+    misaligned, is packed into aligned rows first; the forced plain-load
+    producer reads both as they lie. Every path must give the same bits."""
+    M, N, K = 300, 264, 96      # row strides 16-byte multiples: TMA-able when aligned
     A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 12, "dyadic")
     _, ref32 = oracle.gemm(A, B, C0, 1.0, 1.0, dtype)
     es = 4 if dtype == "tf32" else 2
     flatA = to_dev(np.concatenate([np.zeros(1, A.dtype), A.ravel()]), dtype)
     flatB = to_dev(np.concatenate([np.zeros(1, B.dtype), B.ravel()]), dtype)
+    pa = flatA.data_ptr() + es if "A" in which else to_dev(A, dtype)
+    pb = flatB.data_ptr() + es if "B" in which else to_dev(B, dtype)
     dC = to_dev(C0)
-    with sat.Plan(M, N, K, dtype) as plan:
-        assert "tma" in plan.describe()
-        run(plan, flatA.data_ptr() + es, flatB.data_ptr() + es, dC, 1.0, 1.0)
+    with sat.Plan(M, N, K, dtype, config) as plan:
+        desc = plan.describe()
+        assert ("plain" if config and "plain" in config else "tma") in desc
+        run(plan, pa, pb, dC, 1.0, 1.0)
         torch.cuda.synchronize()
         sat.check(plan.status())
-    checks.assert_bit_exact(dC.cpu().numpy(), ref32, "misaligned")
+    checks.assert_bit_exact(dC.cpu().numpy(), ref32, f"misaligned {which} [{desc}]")
+
+
+# Row strides that are not 16-byte multiples: A through its residue-class
+# views (rows of one class per tile, previous-row elements zeroed), B packed
+# into aligned rows; every row count from one class up, and K tails that
+# leave a class view's last k-block past the end. Dyadic, so bit-exact.
+@pytest.mark.parametrize("config", [None, "256,2,0,4", "256,1,1,2", "128,1,0,8", "256,2,0,2,2", "128,1,0,4,3"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16", "fp16"])
+def test_class_view_rows_dyadic_exact(dtype, config):
+    for i, (M, N, K) in enumerate([(1030, 517, 389), (9, 515, 2049), (515, 1001, 63), (3, 7, 1001),
+                                   (777, 520, 130)]):
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 60 + i, "dyadic")
+        _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+        assert " cls " in desc, desc
+        checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+def test_class_view_with_a_leading_dimension_and_nan_padding():
+    # A with lda = K + 3 (rows misaligned in every class), NaN in the padding
+    # that the views read in front of each row: the fixer must zero it.
+    M, N, K = 600, 300, 250
+    for dtype in ("tf32", "bf16"):
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 70, "dyadic")
+        _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        nan = np.float32("nan") if dtype == "tf32" else (np.uint16(0x7FC0) if dtype == "bf16" else np.float16("nan"))
+        Ap = np.full((M, K + 3), nan, A.dtype)
+        Ap[:, :K] = A
+        dC = to_dev(C0)
+        with sat.Plan(M, N, K, dtype) as plan:
+            plan.run(to_dev(Ap, dtype), to_dev(B, dtype), dC, 1.5, 0.5, stream(), lda=K + 3)
+            torch.cuda.synchronize()
+            sat.check(plan.status())
+            desc = plan.describe()
+        checks.assert_bit_exact(dC.cpu().numpy(), ref32, f"{dtype} lda {K + 3} [{desc}]")
 
 
 @pytest.mark.parametrize("dtype", ["tf32", "bf16"])

@@ -100,10 +100,12 @@ def test_layouts_with_stream_k(ta, tb):
     checks.assert_bit_exact(got, ref32, desc)
 
 
-def test_untransposed_row_strides_off_16_bytes_take_the_plain_path():
+@pytest.mark.parametrize("config", [None, "256,1,0,8,plain"])
+def test_untransposed_row_strides_off_16_bytes(config):
+    # Class views of A and B packed into aligned rows, or the plain loads.
     M, N, K = 150, 264, 96
     dtype = "bf16"
-    A, B, C0, got, desc = _run(M, N, K, dtype, False, False, K + 1, N + 3, N + 1, None, 1.0, 1.0, seed=74)
+    A, B, C0, got, desc = _run(M, N, K, dtype, False, False, K + 1, N + 3, N + 1, config, 1.0, 1.0, seed=74)
     _, ref32 = oracle.gemm(A, B, C0, 1.0, 1.0, dtype)
     checks.assert_bit_exact(got, ref32, desc)
 

@@ -11,6 +11,7 @@ what the first left there (its status word, its split-K partial tiles).
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes when run alone.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -67,8 +68,17 @@ def test_noalloc_matches_gemm_run_on_two_calls(case):
         assert rc == 0, sat.gemm_last_error()
         torch.cuda.synchronize()
         got = out.cpu().numpy()
-        # Same kernel, same choice, fixed K order: the same bits as gemm_run.
-        checks.assert_bit_exact(got, ref_np, f"gemm_run_noalloc call {call + 1} vs gemm_run [{desc}]")
+        # TMA-readable rows: the same kernel, choice and K order as gemm_run,
+        # so the same bits. Rows that TMA cannot address: a plan reads them
+        # through class views (B packed into a copy it allocates), this entry
+        # point through plain loads; the K order then differs, and the two
+        # agree within the dtype's tolerance (bit for bit on dyadic inputs).
+        es = 4 if dtype == "tf32" else 2
+        if (K * es) % 16 == 0 and (N * es) % 16 == 0 or family == "dyadic":
+            checks.assert_bit_exact(got, ref_np, f"gemm_run_noalloc call {call + 1} vs gemm_run [{desc}]")
+        else:
+            checks.assert_rel_rms(got, ref_np.astype(np.float64), si.REL_RMS_BOUND[dtype],
+                                  f"gemm_run_noalloc call {call + 1} vs gemm_run [{desc}]")
         # And the oracle's result: exactly where the inputs are dyadic (one
         # correct answer), within the dtype's rel_rms bound otherwise.
         if family == "dyadic":
