@@ -242,18 +242,32 @@ const char* gemm_last_error(void);
 int gemm_selftest_bounded_wait(uint64_t timeout_ns);
 
 /*
- * The GEMM as a device routine inside a kernel of the library's own: the
- * routine (sat::gemm_cta in gemm_kernel.cuh, callable by any kernel that
- * meets the conditions stated there) computes C = alpha * A * B + beta * C
- * as phase 1 of a persistent kernel, whose phase 2, in the same launch,
- * replaces each element of the tiles the CTA produced by max(x, 0). Dense
- * row-major operands, 16-byte aligned with 16-byte-multiple row strides
- * (GEMM_ERR_ALIGN otherwise); 1-SM 128 x 128 tiles; no error word, so a
- * bounded wait that gives up shows only in the result. For tests: it shows
- * that the routine composes with other work in one launch.
+ * Prepare the device-routine form of the GEMM (include/gemm_device.cuh) for
+ * C = alpha * A * B + beta * C on the CURRENT device: writes a
+ * gemm_device_params (tensor maps of A, B and C, the persistent schedule,
+ * and the launch shape: threads, dynamic shared memory, cluster size, grid)
+ * into `params` (host memory, at least `params_bytes` bytes, 64-byte
+ * aligned). cta_group 1 selects the 1-SM 128 x 128 tile, 2 the CTA-pair
+ * 256 x 256 tile. Dense row-major operands in device memory, 16-byte aligned,
+ * with row strides that are multiples of 16 bytes and N a multiple of 4
+ * (GEMM_ERR_ALIGN otherwise). The params hold device pointers only; nothing
+ * is allocated. The routine has no error word: a bounded wait that gives up
+ * shows only in the result. Returns 0 or a negative gemm_status_t.
+ */
+int gemm_device_prepare(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const void* A, const void* B, float* C,
+                        float alpha, float beta, int cta_group, void* params, int64_t params_bytes);
+
+/*
+ * The device routine inside a kernel of the library's own: a persistent
+ * kernel prepared by gemm_device_prepare() whose phase 1 is
+ * gemm_device_run (C = alpha * A * B + beta * C) and whose phase 2, in the
+ * same launch, replaces each element of the tiles the CTA produced by
+ * max(x, 0). cta_group as for gemm_device_prepare (1: 128 x 128 tiles,
+ * 2: CTA pairs, 256 x 256). For tests: it shows that the routine composes
+ * with other work in one launch, for either tile.
  */
 int gemm_selftest_device_call(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const void* A, const void* B,
-                              float* C, float alpha, float beta, void* cuda_stream);
+                              float* C, float alpha, float beta, int cta_group, void* cuda_stream);
 
 /*
  * Host-only view of the dispatcher (no device is touched): the choice that

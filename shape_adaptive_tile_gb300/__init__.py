@@ -26,6 +26,7 @@ STATUS = {0: "GEMM_OK", -1: "GEMM_ERR_ARG", -2: "GEMM_ERR_ARCH", -3: "GEMM_ERR_A
 EXPORTS = ("gemm_plan_create", "gemm_plan_create_config", "gemm_plan_create_ex", "gemm_run", "gemm_run_ex",
            "gemm_run_host", "gemm_plan_destroy", "gemm_plan_status", "gemm_plan_describe", "gemm_last_error",
            "gemm_selftest_bounded_wait", "gemm_select_config", "gemm_run_noalloc", "gemm_selftest_device_call",
+           "gemm_device_prepare",
            "rowop_softmax", "rowop_rmsnorm", "rowop_layernorm")
 
 _lock = threading.Lock()
@@ -70,8 +71,10 @@ def lib() -> ctypes.CDLL:
             L.gemm_selftest_bounded_wait.argtypes = [ctypes.c_uint64]
             L.gemm_selftest_bounded_wait.restype = i32
             L.gemm_run_noalloc.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
-            L.gemm_selftest_device_call.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, vp]
+            L.gemm_selftest_device_call.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, i32, vp]
             L.gemm_selftest_device_call.restype = i32
+            L.gemm_device_prepare.argtypes = [i64, i64, i64, i32, vp, vp, vp, f32, f32, i32, vp, i64]
+            L.gemm_device_prepare.restype = i32
             L.rowop_softmax.argtypes = [vp, i64, vp, i64, i64, i64, vp]
             L.rowop_softmax.restype = i32
             L.rowop_rmsnorm.argtypes = [vp, i64, vp, vp, i64, i64, i64, f32, vp]
@@ -146,9 +149,17 @@ def gemm_run_noalloc(M: int, N: int, K: int, dtype, A, B, C, alpha: float = 1.0,
 
 
 def gemm_selftest_device_call(M: int, N: int, K: int, dtype, A, B, C, alpha: float = 1.0, beta: float = 0.0,
-                              stream=None) -> int:
+                              cta_group: int = 1, stream=None) -> int:
     """GEMM then ReLU in one launch, the GEMM being the device-callable routine (see include/gemm.h)."""
-    return lib().gemm_selftest_device_call(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, _p(stream))
+    return lib().gemm_selftest_device_call(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, cta_group,
+                                           _p(stream))
+
+
+def gemm_device_prepare(M: int, N: int, K: int, dtype, A, B, C, alpha: float, beta: float, cta_group: int,
+                        params, params_bytes: int) -> int:
+    """Fill the device routine's launch parameters into host memory `params` (see include/gemm.h)."""
+    return lib().gemm_device_prepare(M, N, K, _dt(dtype), _p(A), _p(B), _p(C), alpha, beta, cta_group, _p(params),
+                                     params_bytes)
 
 
 # ---- row operators (include/rowops.h) -----------------------------------------

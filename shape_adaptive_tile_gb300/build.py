@@ -41,7 +41,7 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
-    files += [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h")]
+    files += [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h"), os.path.join(INCLUDE, "gemm_device.cuh")]
     return [f for f in files if os.path.isfile(f)]
 
 

@@ -11,7 +11,9 @@ import pytest
 import shape_adaptive_tile_gb300 as sat
 
 INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
-HEADERS = [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h")]
+HEADERS = [os.path.join(INCLUDE, "gemm.h"), os.path.join(INCLUDE, "rowops.h")]  # the C ABI
+# (include/gemm_device.cuh is the device routine's CUDA C++ header; the library
+# builds it into gemm_selftest_device_call.)
 
 
 @pytest.fixture(scope="module")

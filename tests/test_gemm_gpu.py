@@ -192,16 +192,48 @@ def test_swapped_operands_with_c_not_16_byte_aligned():
 # The GEMM as a device routine: phase 1 of a kernel whose phase 2 (same
 # launch) applies max(x, 0) to the tiles each CTA produced. 48 tiles (one
 # per CTA) and 176 tiles (more than the SMs: the persistent loop).
-@pytest.mark.parametrize("M,N,K", [(700, 1000, 520), (2000, 1400, 264)])
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(700, 1000, 520), (2000, 1400, 264), (5000, 4100, 136)])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_device_callable_gemm_inside_a_megakernel(dtype, M, N, K):
+def test_device_callable_gemm_inside_a_megakernel(dtype, M, N, K, cta_group):
+    # GEMM then ReLU in one launch, the GEMM being the public device routine
+    # (include/gemm_device.cuh), 1-SM 128 x 128 tiles or CTA pairs of
+    # 256 x 256; (5000, 4100, 136) has more tiles than co-resident blocks.
     A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 91, "dyadic")
     _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, dtype)
     dC = to_dev(C0)
     assert sat.gemm_selftest_device_call(M, N, K, dtype, to_dev(A, dtype), to_dev(B, dtype), dC, 1.5, -0.5,
-                                         stream()) == 0, sat.gemm_last_error()
+                                         cta_group, stream()) == 0, sat.gemm_last_error()
     torch.cuda.synchronize()
-    checks.assert_bit_exact(dC.cpu().numpy(), np.maximum(ref32, np.float32(0)), f"{dtype} {M}x{N}x{K} fused relu")
+    checks.assert_bit_exact(dC.cpu().numpy(), np.maximum(ref32, np.float32(0)),
+                            f"{dtype} {M}x{N}x{K} cta_group {cta_group} fused relu")
+
+
+def test_device_prepare_fills_the_launch_shape():
+    import ctypes
+    M, N, K = 2000, 1400, 264
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(K, N, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(M, N, device="cuda")
+    buf = (ctypes.c_uint8 * 4096)()
+    base = ctypes.addressof(buf)
+    ptr = (base + 63) // 64 * 64
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for cg in (1, 2):
+        assert sat.gemm_device_prepare(M, N, K, "bf16", A, B, C, 1.0, 0.0, cg, ptr, 4096 - (ptr - base)) == 0
+        # The launch shape (threads, smem, cluster, grid, bn, cta_group) closes
+        # the struct, after three 128-byte tensor maps and the arguments.
+        tail = list((ctypes.c_int * 1000).from_address(ptr))
+        bn = 256 if cg == 2 else 128
+        found = [i for i in range(96, 994) if tail[i] == 320 and tail[i + 2] == cg and tail[i + 4] == bn
+                 and tail[i + 5] == cg]
+        assert len(found) == 1, "launch shape not found"
+        threads, smem, cluster, grid = tail[found[0]:found[0] + 4]
+        assert threads == 320 and 200000 < smem <= 232448 and cluster == cg
+        tiles = -(-M // (128 * cg)) * -(-N // bn)
+        assert grid == min(tiles, sms // cg) * cg
+    assert sat.gemm_device_prepare(M, N, K, "bf16", A, B, C, 1.0, 0.0, 3, ptr, 4096) == -1
+    assert sat.gemm_device_prepare(M, N, K, "bf16", A, B, C, 1.0, 0.0, 1, ptr + 8, 4096) == -3
 
 
 def test_k_zero_and_alpha_zero_scale_c():
