@@ -193,12 +193,12 @@ def test_swapped_operands_with_c_not_16_byte_aligned():
 # launch) applies max(x, 0) to the tiles each CTA produced. 48 tiles (one
 # per CTA) and 176 tiles (more than the SMs: the persistent loop).
 @pytest.mark.parametrize("cta_group", [1, 2])
-@pytest.mark.parametrize("M,N,K", [(700, 1000, 520), (2000, 1400, 264), (5000, 4100, 136)])
+@pytest.mark.parametrize("M,N,K", [(700, 1000, 520), (2000, 1400, 264), (5000, 4104, 136)])
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_device_callable_gemm_inside_a_megakernel(dtype, M, N, K, cta_group):
     # GEMM then ReLU in one launch, the GEMM being the public device routine
     # (include/gemm_device.cuh), 1-SM 128 x 128 tiles or CTA pairs of
-    # 256 x 256; (5000, 4100, 136) has more tiles than co-resident blocks.
+    # 256 x 256; (5000, 4104, 136) has more tiles than co-resident blocks.
     A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 91, "dyadic")
     _, ref32 = oracle.gemm(A, B, C0, 1.5, -0.5, dtype)
     dC = to_dev(C0)
