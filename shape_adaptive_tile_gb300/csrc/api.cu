@@ -91,6 +91,7 @@ struct Scratch {
     float* sk_ws = nullptr;            // stream-K: one 128 x bn float partial tile per CTA
     unsigned* sk_flags = nullptr;      // stream-K: one counter per CTA, then the ticket counter
     unsigned epoch = 0;                // stream-K launches on these counters since they were cleared
+    unsigned long long sk_sig = 0;     // the stream-K layout those launches used
     void* bpack = nullptr;             // B with 16-byte-aligned rows (K x ldb_pack elements), when B's are not
     cudaEvent_t done = nullptr;        // recorded after each run that used this set
     unsigned long long last_use = 0;
@@ -320,6 +321,7 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         p->cls = sat::find_entry(dt, bn, c.cg, sat::kProdClassA);
         if (p->cls)
             p->slots_cls = slots_for(p, p->cls);
+
         p->ldb_pack = (N * es + 15) / 16 * 16 / es;
     }
     for (const sat::KernelEntry* k : {p->tma, p->plain, p->plain_strided, p->cls}) {
@@ -365,6 +367,12 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             p->sk_bn = t->bn;
             p->grid_tma = p->sk_ctas;
         }
+    }
+    // Class-view runs lay out stream-K per run (their tiles depend on A's
+    // alignment); size the scratch for their grid too.
+    if (p->cls && c.sk && p->splits == 1) {
+        p->sk_ctas = std::max<int>(p->sk_ctas, static_cast<int>(p->slots_cls * p->cls->cg));
+        p->sk_bn = std::max(p->sk_bn, p->cls->bn);
     }
     if (e != cudaSuccess) {
         cuda_fail(e, "allocating the host-mapped error word");
@@ -439,7 +447,7 @@ int acquire_scratch(const gemm_plan* p, cudaStream_t stream, bool want_pack, Scr
                           CU_TENSOR_MAP_SWIZZLE_128B) == 0)
                 s.ws_tma = true;
         }
-        if (e == cudaSuccess && p->sk_tiles > 0) {
+        if (e == cudaSuccess && p->sk_ctas > 0) {
             e = cudaMalloc(&s.sk_ws, static_cast<size_t>(p->sk_ctas) * 128 * p->sk_bn * sizeof(float));
             if (e == cudaSuccess)
                 e = cudaMalloc(&s.sk_flags, sk_flag_bytes(p));
@@ -621,7 +629,13 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     a.num_tiles = a.tiles_m * a.tiles_n * a.splits;
     a.out_rows = static_cast<int>(p->M);
     const bool split = splits > 1;
-    const bool sk = use_tma && p->sk_tiles > 0;
+    // Stream-K: the plan's layout for TMA runs; for class-view runs one laid
+    // out here, over their own tiles and k-blocks.
+    int sk_tiles = use_tma ? p->sk_tiles : 0, sk_w = use_tma ? p->sk_w : 0;
+    if (use_cls && p->choice.sk && !split && p->sk_ctas >= p->slots_cls * k->cg &&
+        !sat::sk_layout(tiles_m * tiles_n, a.num_kb, p->slots_cls, &sk_tiles, &sk_w))
+        sk_tiles = sk_w = 0;
+    const bool sk = sk_tiles > 0;
     const bool pack = use_cls && !b_rows_ok;
     // Split-K and stream-K runs, and class-view runs whose B must be packed,
     // write this stream's scratch set, held (with the plan's scratch lock)
@@ -663,15 +677,24 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         // is written, and the ticket counter number x slots once every slot of
         // it is handed out. Before the counters could wrap, they are cleared
         // and numbering restarts.
+        // A slot's counter counts its partial tiles over the launches on these
+        // counters, so every launch must use one layout: a different one (a
+        // class-view run after a TMA run, or another alignment of A) clears
+        // them first, on the stream, and numbering restarts.
+        const unsigned long long sig = (static_cast<unsigned long long>(use_cls ? 1 : 0) << 63) ^
+                                       (static_cast<unsigned long long>(sk_tiles) << 32) ^
+                                       (static_cast<unsigned long long>(sk_w) << 8) ^
+                                       static_cast<unsigned long long>(a.tiles_m);
         unsigned epoch = ++sc->epoch;
-        if (epoch >= (1u << 28)) {
+        if (epoch >= (1u << 28) || sc->sk_sig != sig) {
             e = cudaMemsetAsync(sc->sk_flags, 0, sk_flag_bytes(p), stream);
             if (e != cudaSuccess)
                 return cuda_fail(e, "clearing the stream-K counters");
             sc->epoch = epoch = 1;
+            sc->sk_sig = sig;
         }
-        a.sk_tiles = p->sk_tiles;
-        a.sk_w = p->sk_w;
+        a.sk_tiles = sk_tiles;
+        a.sk_w = sk_w;
         a.sk_ws = sc->sk_ws;
         a.sk_flags = sc->sk_flags;
         a.sk_ticket = sc->sk_flags + p->sk_ctas + kTicketPad - 1;
@@ -763,8 +786,11 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
             for (int r = 0; r < a.a_classes; ++r)
                 cmaps[r] = p->tmCls[r];
         }
+        // Every slot runs under stream-K; otherwise one block (pair) per unit, at
+        // most the co-resident ones.
         const int64_t units = static_cast<int64_t>(a.num_tiles);
-        const int grid = static_cast<int>((units < p->slots_cls ? units : p->slots_cls) * k->cg);
+        const int grid =
+            static_cast<int>((sk || units >= p->slots_cls ? p->slots_cls : units) * k->cg);
         e = k->launch(cmaps, &tmB, &tmC, &a, grid, stream);
     } else {
         e = k->launch(&tmA, &tmB, &tmC, &a, use_tma ? p->grid_tma : p->grid_plain, stream);

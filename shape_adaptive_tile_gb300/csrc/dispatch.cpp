@@ -194,7 +194,6 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
             // class-view tiles: 1-SM 128 or 256 columns, CTA-pair 256
             c.swap = 0;
             c.stages = 0;
-            c.sk = 0;
             if (c.cg == 2)
                 c.bn = 256;
         }
@@ -310,6 +309,9 @@ Choice select_config(int64_t M, int64_t N, int64_t K, int dt, int sm_count, bool
     // idle share is worth at least 3% of the run, and K is long enough for
     // the fix-up of a split tile (one partial tile written and read per
     // contributor) to be small against a tile's K loop.
+    // (Not for class-view tiles, tma_ok false: their stream-K pieces end in the
+    // row-store epilogue, measured 1.4-1.7x slower than whole tiles at
+    // (8191, 4097, 2049).)
     if (best.splits == 1 && tma_ok) {
         const int64_t tiles = tiles_of(best.bn, best.cg, best.swap);
         const int64_t slots = std::max<int64_t>(1, sm_count / best.cg);

@@ -892,7 +892,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
             const bool late_c = SK && !T::SWAP && c_tma && beta != 0.0f;
             // Row-store path (C not 16-byte aligned), beta != 0: each chunk's
             // 32 rows of C at this lane's column are loaded together, all in
-            // flight at once.
+            // flight at once, the first chunk's before the accumulator wait.
             const bool rows_c = MODE == 0 && !T::SWAP && !c_tma && beta != 0.0f;
             // C through the ring: where the next unit's stages start, and per
             // stage the parity of its next C fill.
@@ -922,8 +922,20 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                 // its latency overlaps the main loop; later chunks read theirs in turn.
                 float cv[32];
                 if constexpr (!RING) {
-                    if (prefetch_c)
+                    if (prefetch_c) {
                         load_c(cv, row0 + lane, n0 + half * 32);
+                    } else if (rows_c) {
+                        // Row-store path: the first chunk's 32 rows at this
+                        // lane's column, loaded before the accumulator wait too.
+                        const int col = n0 + half * 32 + lane;
+                        const int64_t rb =
+                            (static_cast<int64_t>(yoff) + (T::CLS ? cls + ncls * row0 : row0)) * ldc + col;
+                        const int64_t rs = T::CLS ? static_cast<int64_t>(ncls) * ldc : static_cast<int64_t>(ldc);
+                        const int nr = T::CLS ? min(32, args.a_rows[cls] - row0) : min(32, args.M - row0);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            cv[i] = i < nr && col < args.N ? c_load(args.C, args.c_half, rb + i * rs) : 0.0f;
+                    }
                 }
                 if (!wait_bar<false>(tfull_bar(acc), acc_phase, wc, kErrTimeoutEpilogue))
                     break;
@@ -1146,7 +1158,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                     // flight at once (the accumulator values now sit in the
                     // buffer, which frees their registers).
                     if constexpr (!RING) {
-                        if (rows_c) {
+                        if (rows_c && c != half) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i)
                                 cv[i] = i < nrows && col < args.N ? c_load(args.C, args.c_half, c0 + i * rstep) : 0.0f;

@@ -46,7 +46,7 @@ def candidates(M, N, K, dtype, tma_ok, sm_count=152, beta=0.0):
         for raster, group in itertools.product((0, 1), (1, 2, 4, 8, 16)):
             out.append(f"{bn},{cg},{raster},{group}")
             # stream-K where more than a wave of tiles ends in a partial one
-            if tma_ok and tiles > slots and tiles % slots:
+            if tiles > slots and tiles % slots:
                 out.append(f"{bn},{cg},{raster},{group},sk")
             # beta != 0: also with the epilogue loading C itself instead of
             # the producer fetching it through the ring (the 1-SM 256-wide

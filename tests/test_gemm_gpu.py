@@ -287,16 +287,41 @@ def test_misaligned_pointers(dtype, config, which):
 # views (rows of one class per tile, previous-row elements zeroed), B packed
 # into aligned rows; every row count from one class up, and K tails that
 # leave a class view's last k-block past the end. Dyadic, so bit-exact.
-@pytest.mark.parametrize("config", [None, "256,2,0,4", "256,1,1,2", "128,1,0,8", "256,2,0,2,2", "128,1,0,4,3"])
+@pytest.mark.parametrize("config", [None, "256,2,0,4", "256,1,1,2", "128,1,0,8", "256,2,0,2,2", "128,1,0,4,3",
+                                    "256,2,0,4,sk", "128,1,1,2,sk"])
 @pytest.mark.parametrize("dtype", ["tf32", "bf16", "fp16"])
 def test_class_view_rows_dyadic_exact(dtype, config):
+    # (3000, 2049, 1031) and (2500, 3001, 777) make several waves of class
+    # tiles with a partial last one: stream-K pieces where the config asks.
     for i, (M, N, K) in enumerate([(1030, 517, 389), (9, 515, 2049), (515, 1001, 63), (3, 7, 1001),
-                                   (777, 520, 130)]):
+                                   (777, 520, 130), (3000, 2049, 1031), (2500, 3001, 777)]):
         A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 60 + i, "dyadic")
         _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
         got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
         assert " cls " in desc, desc
         checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+
+
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_stream_k_plan_alternating_tma_and_class_view_runs(dtype):
+    # One stream-K plan, one stream: runs on aligned operands (TMA, the plan's
+    # layout) and on A one element off (class views, a layout of their own)
+    # share the stream's counters, which a change of layout clears.
+    M, N, K = 2560, 2560, 1024
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 80, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    es = 4 if dtype == "tf32" else 2
+    dA, dB = to_dev(A, dtype), to_dev(B, dtype)
+    flatA = to_dev(np.concatenate([np.zeros(1, A.dtype), A.ravel()]), dtype)
+    with sat.Plan(M, N, K, dtype, "256,2,0,4,sk") as plan:
+        desc = plan.describe()
+        assert " sk" in desc, desc
+        for i, pa in enumerate([dA, flatA.data_ptr() + es, dA, dA, flatA.data_ptr() + es, flatA.data_ptr() + es, dA]):
+            dC = to_dev(C0)
+            run(plan, pa, dB, dC, 1.5, 0.5)
+            torch.cuda.synchronize()
+            checks.assert_bit_exact(dC.cpu().numpy(), ref32, f"run {i} [{desc}]")
+        sat.check(plan.status())
 
 
 def test_class_view_with_a_leading_dimension_and_nan_padding():
