@@ -80,6 +80,9 @@ gemm_plan* gemm_plan_create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype)
  * group >= 1; splits 1..16 K splits, default 1), optionally followed by
  * ",st<n>" (a ring of n shared-memory stages where the untransposed TMA
  * kernel of that tile is compiled with that depth; the deepest by default),
+ * ",fwd" (every wave of tiles runs through K forwards; by default alternate
+ * waves run it backwards, starting on the operand panels the previous wave
+ * left in L2; either order is fixed per tile, so results repeat bit for bit),
  * ",cload" (with beta != 0 the epilogue loads C itself instead of the
  * producer fetching it through the operand ring), ",swap" (operand roles
  * exchanged: the tensor core computes C^T = B^T A^T in tiles of 128 columns

@@ -110,6 +110,7 @@ struct gemm_plan {
     int c_half = 0;                         // element type of C: 0 fp32, 1 bf16, 2 fp16
     sat::Choice choice{};
     bool force_plain = false;
+    bool alt_k = true;    // alternate waves run through K in opposite directions
     bool c_ring = false;  // beta != 0: the producer fetches C through the operand ring
     const sat::KernelEntry* tma = nullptr;    // null when the strides rule out TMA
     const sat::KernelEntry* plain = nullptr;  // 1-SM plain-load variant (misaligned pointers)
@@ -240,8 +241,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         // Optional tags after the numbers, in any order: ",cload" (the
         // epilogue loads C itself), ",sk" (stream-K), ",plain" (plain-load
         // producer). Each is looked up first; the numbers end at the first.
-        char* tag[5] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain"),
-                        std::strstr(head, ",swap"), std::strstr(head, ",st")};
+        char* tag[6] = {std::strstr(head, ",cload"), std::strstr(head, ",sk"), std::strstr(head, ",plain"),
+                        std::strstr(head, ",swap"), std::strstr(head, ",st"), std::strstr(head, ",fwd")};
+        // ",fwd": every wave runs through K forwards (no alternating direction).
+        p->alt_k = tag[5] == nullptr;
         const bool cload = tag[0] != nullptr, sk = tag[1] != nullptr, swap = tag[3] != nullptr;
         p->force_plain = tag[2] != nullptr;
         // ",st<n>": a ring of n stages (a compiled depth of the TMA kernel).
@@ -397,6 +400,8 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
                   p->tma ? p->grid_tma : p->cls ? static_cast<int>(p->slots_cls * p->cls->cg) : p->grid_plain,
                   source, p->c_ring ? " cring" : "", sk_desc, p->tma && p->tma->prod == sat::kProdSwap ? " swap" : "",
                   trans_a ? " ta" : "", trans_b ? " tb" : "");
+    if (!p->alt_k)
+        std::snprintf(p->desc + std::strlen(p->desc), sizeof p->desc - std::strlen(p->desc), " fwd");
     if (c_type)
         std::snprintf(p->desc + std::strlen(p->desc), sizeof p->desc - std::strlen(p->desc), " c%s",
                       c_type == 1 ? "bf16" : "fp16");
@@ -660,6 +665,7 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     }
     a.group = p->choice.group;
     a.raster = p->choice.raster;
+    a.alt_k = p->alt_k ? 1 : 0;
     a.err = p->d_err;
     a.timeout_ns = p->timeout_ns;
 

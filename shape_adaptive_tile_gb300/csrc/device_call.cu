@@ -126,6 +126,7 @@ extern "C" int gemm_device_prepare(int64_t M, int64_t N, int64_t K, gemm_dtype_t
     a.out_rows = static_cast<int>(M);
     a.group = 8;
     a.raster = 0;
+    a.alt_k = 1;
     a.c_tma = 1;
     a.timeout_ns = 2000000000ull;
 

@@ -45,6 +45,7 @@ struct GemmArgs {
     int raster;                // 0: groups along M, 1: groups along N
     int c_tma;                 // 1: C is written (and read) through the TMA store path
     int c_ring;                // 1: the producer also fetches each tile's C (beta != 0) through the ring
+    int alt_k;                 // 1: alternate waves of whole units run through K in opposite directions
     // Stream-K (sk_tiles > 0; only with splits == 1): the first sk_tiles tiles
     // in raster order are cut into k-block ranges of sk_w consecutive
     // positions of the (tile, k-block) sequence, one range per CTA slot

@@ -175,8 +175,9 @@ __device__ __forceinline__ uint32_t swz_kmajor(int r, int k)
 // own, and only on each one's first unit.
 constexpr int kWhole = 0, kSkPartial = 1, kSkFinal = 2;
 
+// rev: the unit runs its k-blocks from kb1 - 1 down to kb0 (see work_next).
 struct Unit {
-    int tm, tn, s, kb0, kb1, kind, first;
+    int tm, tn, s, kb0, kb1, kind, first, rev;
 };
 
 __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
@@ -189,6 +190,7 @@ __device__ __forceinline__ Unit unit_coord(int u, const GemmArgs& a)
     w.kb1 = min(a.num_kb, w.kb0 + a.kb_per_split);
     w.kind = kWhole;
     w.first = 0;
+    w.rev = 0;
     return w;
 }
 
@@ -229,11 +231,19 @@ __device__ __forceinline__ bool work_next(const GemmArgs& a, int G, WorkIter& it
         w.kb1 = it.end - tstart;
         w.kind = w.kb1 < a.num_kb ? kSkPartial : (w.kb0 > 0 ? kSkFinal : kWhole);
         w.first = tstart / a.sk_w;   // the slot whose range holds the tile's k-block 0
+        w.rev = 0;
         it.end = p0;
         return true;
     }
     if (it.t < a.num_tiles) {
         w = unit_coord(it.t, a);
+        // Alternate waves of whole units run through K in opposite directions
+        // (a.alt_k): a wave whose panels exceed L2 leaves the last k-blocks
+        // it read there, which the next wave, reversed, reads first. After
+        // stream-K pieces (which end on tiles' last k-blocks) the first wave
+        // is a reversed one. The order depends only on the layout, so it is
+        // the same on every run.
+        w.rev = a.alt_k ? (((it.t - a.sk_tiles) / G) + (a.sk_tiles > 0 ? 1 : 0)) & 1 : 0;
         it.t += G;
         return true;
     }
@@ -441,7 +451,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                     const int tmv = T::CLS ? w.tm / args.a_classes : w.tm;
                     const int m0 = tmv * (T::BM * CG) + static_cast<int>(rank) * T::BM;
                     const int n0 = w.tn * BN + static_cast<int>(rank) * T::BN_CTA;
-                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    for (int i = 0; i < w.kb1 - w.kb0; ++i) {
+                        const int kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
                         if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                             ok = false;
                             break;
@@ -572,7 +583,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
             while (ok && work_next(args, tile_step, it, w)) {
                 const int m0 = w.tm * T::BM;
                 const int n0 = w.tn * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int i = 0; i < w.kb1 - w.kb0; ++i) {
+                    const int kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
                     if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                         ok = false;
                         break;
@@ -650,7 +662,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
             while (ok && work_next(args, tile_step, it, w)) {
                 const int m0 = w.tm * T::BM;
                 const int n0 = w.tn * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int i = 0; i < w.kb1 - w.kb0; ++i) {
+                    const int kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
                     if (!wait_bar<false>(empty_bar(stage), phase ^ 1u, wc, kErrTimeoutProducer)) {
                         ok = false;
                         break;
@@ -744,7 +757,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                 // by the peer's fixer (plain stores, then a cluster-scope fence
                 // and complete_tx), so that wait acquires at cluster scope.
                 const bool fix0 = T::CLS && CG == 2 && w.kb0 == 0 && args.a_shift[w.tm % args.a_classes] > 0;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int i = 0; i < w.kb1 - w.kb0; ++i) {
+                    const int kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
                     const bool got = fix0 && kb == 0
                                          ? wait_bar<kClu>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma)
                                          : wait_bar<false>(full_bar(stage), (fpar >> stage) & 1u, wc, kErrTimeoutMma);
@@ -765,7 +779,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                                                     : sdesc(a0 + ks * T::K_KSTEP, 16, 1024, kLayoutSW128);
                         const uint64_t bd = T::B_KM ? sdesc(b0 + ks * T::K_KSTEP, 16, 1024, kLayoutSW128)
                                                     : sdesc(b0 + ks * T::MN_KSTEP, T::MN_LBO, T::MN_SBO, T::MN_LAYOUT);
-                        mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (kb != w.kb0 || ks != 0) ? 1u : 0u);
+                        mma_ss<CG, T::kTF32>(d, ad, bd, T::IDESC, (i != 0 || ks != 0) ? 1u : 0u);
                     }
                     issued = true;
                     if constexpr (CG == 1)
@@ -824,10 +838,13 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
             while (work_next(args, tile_step, it, w)) {
                 const int ashift = args.a_shift[w.tm % args.a_classes];
                 if (w.kb0 == 0 && ashift > 0) {
-                    if (!wait_bar<false>(afix_bar(stage), (apar >> stage) & 1u, wc, kErrTimeoutProducer))
+                    // k-block 0 is the unit's first stage, or its last when the
+                    // unit runs through K backwards.
+                    const int fs = w.rev ? (stage + (w.kb1 - w.kb0 - 1)) % T::STAGES : stage;
+                    if (!wait_bar<false>(afix_bar(fs), (apar >> fs) & 1u, wc, kErrTimeoutProducer))
                         break;
-                    apar ^= 1u << stage;
-                    const uint32_t a0 = sA + stage * T::A_BYTES;
+                    apar ^= 1u << fs;
+                    const uint32_t a0 = sA + fs * T::A_BYTES;
                     for (int i = lane; i < T::BM * ashift; i += 32) {
                         const int row = i / ashift, k = i - row * ashift;
                         if constexpr (T::ES == 4)
@@ -839,7 +856,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                     __syncwarp();
                     if (lane == 0) {
                         fence_acq_rel_cluster();
-                        mbar_complete_tx_cluster(full0 + 8u * stage, T::A_BYTES);
+                        mbar_complete_tx_cluster(full0 + 8u * fs, T::A_BYTES);
                     }
                     __syncwarp();
                 }

@@ -230,6 +230,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     a.out_rows = splits > 1 ? static_cast<int>(ws_rows) : static_cast<int>(M);
     a.group = c.group;
     a.raster = c.raster;
+    a.alt_k = 1;
     a.err = status;
     a.timeout_ns = 2000000000ull;
 

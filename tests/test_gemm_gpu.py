@@ -302,6 +302,25 @@ def test_class_view_rows_dyadic_exact(dtype, config):
         checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
 
 
+@pytest.mark.parametrize("config", ["128,1,0,4,plain", "256,1,1,2,plain", "128,1,0,4", "256,2,1,2",
+                                    "256,2,0,4,fwd", "128,1,0,4,2"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_waves_through_k_in_both_directions(dtype, config):
+    # Two and more waves of tiles: by default alternate waves run through K
+    # backwards (every producer kind, the MMA's first accumulate, split-K
+    # slices); ",fwd" keeps every wave forwards. Exact on dyadic inputs either
+    # way, within tolerance on Gaussian ones.
+    M, N, K = 3000, 2560, 520
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 81, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+    checks.assert_bit_exact(got, ref32, f"{dtype} [{desc}]")
+    A, B, C0 = si.problem(M, N, K, dtype, "normal", 82, "normal")
+    ref64, _ = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+    checks.assert_rel_rms(got, ref64, si.REL_RMS_BOUND[dtype], f"{dtype} gaussian [{desc}]")
+
+
 @pytest.mark.parametrize("dtype", ["tf32", "bf16"])
 def test_stream_k_plan_alternating_tma_and_class_view_runs(dtype):
     # One stream-K plan, one stream: runs on aligned operands (TMA, the plan's
