@@ -58,11 +58,20 @@ __device__ __forceinline__ float block_reduce(float v, float (*scratch)[NW], int
     return t;
 }
 
+// CTAs of NT threads holding PER values each that the launch bounds ask to
+// fit on one SM at once: rows of 32 values per thread in 16-byte vectors
+// otherwise leave the compiler free to take more registers than two
+// 512-thread (three 256-thread) CTAs can share, and an SM then holds one row
+// where it could hold two. (The 4-byte variants would spill under that bound;
+// 0 leaves the other variants unconstrained.)
+template <int NT, int PER, int VEC>
+constexpr int kRowMinBlocks = PER == 32 && VEC == 4 ? (NT == 512 ? 2 : NT == 256 ? 3 : 0) : 0;
+
 // NT threads (one CTA) take a row; element e of a thread's share is column
 // e / VEC * NT * VEC + threadIdx.x * VEC + e % VEC. VEC = 4 loads 16 bytes
 // at a time.
 template <int OP, int NT, int PER, int VEC>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, (kRowMinBlocks<NT, PER, VEC>))
     sat_rowop_kernel(const float* X, int64_t ldx, const float* __restrict__ gamma,
                      const float* __restrict__ beta, float* Y, int64_t ldy, int64_t rows, int width,
                      float eps)
