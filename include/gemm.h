@@ -125,11 +125,17 @@ gemm_plan* gemm_plan_create_ex(int64_t M, int64_t N, int64_t K, gemm_dtype_t dty
  *      (so with beta == 0 any contents, NaN included, are ignored).
  * M == 0 or N == 0: nothing is done. K == 0 or alpha == 0: C = beta * C.
  * A and B must be aligned to their element size, C to 4 bytes
- * (GEMM_ERR_ALIGN otherwise); 16-byte aligned A/B with 16-byte-multiple row
- * strides take the TMA load path, anything else the plain-load path, with
- * identical results. A plan that splits K launches a second kernel on the
- * same stream that sums the partial tiles in fixed order and applies alpha
- * and beta.
+ * (GEMM_ERR_ALIGN otherwise). Rows that TMA can address (16-byte aligned
+ * starts) are read as they lie. Otherwise (untransposed plans): A is read
+ * through one tensor map per residue class of its row starts modulo 16
+ * bytes, and B is first copied, by a kernel on the same stream, into rows of
+ * whole 128-byte lines in scratch of the stream's own (allocated by the
+ * plan's first such run on that stream). Every path sums K in a fixed
+ * order; the class views start their k-blocks a few elements earlier, so
+ * their results can differ from the aligned path's by rounding (and are
+ * identical where every partial sum is exact). A plan that splits K launches
+ * a second kernel on the same stream that sums the partial tiles in fixed
+ * order and applies alpha and beta.
  * Threading: one plan may run on several streams, from several threads, at
  * once. A split-K or stream-K plan keeps its partial tiles in scratch of the
  * stream's own (allocated by the plan's first run on that stream, so make
@@ -152,9 +158,11 @@ int gemm_run(const gemm_plan* plan, const void* A, const void* B, float* C, floa
  * stored (>= K, or >= M when the plan has A transposed), ldb for B as stored
  * (>= N, or >= K when transposed), ldc for C (>= N, in elements of the
  * plan's C type; C points to elements of that type, aligned to their size).
- * gemm_run is this call with the dense strides. Operands whose row strides are not
- * 16-byte multiples take the plain-load path (untransposed plans only); C
- * whose row stride is not a 16-byte multiple takes the row-store epilogue.
+ * gemm_run is this call with the dense strides. Operand rows that TMA cannot
+ * address (strides that are not 16-byte multiples) take the class views of A
+ * and the packed copy of B described at gemm_run (untransposed plans only;
+ * a transposed plan returns GEMM_ERR_ALIGN for them); C whose base or row
+ * stride is not a 16-byte multiple takes the row-store epilogue.
  * GEMM_ERR_ARG for a stride below the minimum.
  */
 int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,

@@ -92,7 +92,7 @@ struct Scratch {
     unsigned* sk_flags = nullptr;      // stream-K: one counter per CTA, then the ticket counter
     unsigned epoch = 0;                // stream-K launches on these counters since they were cleared
     unsigned long long sk_sig = 0;     // the stream-K layout those launches used
-    void* bpack = nullptr;             // B with 16-byte-aligned rows (K x ldb_pack elements), when B's are not
+    void* bpack = nullptr;             // B in rows of whole 128-byte lines (K x ldb_pack elements), when its own rows are not TMA-addressable
     cudaEvent_t done = nullptr;        // recorded after each run that used this set
     unsigned long long last_use = 0;
 };
@@ -307,6 +307,10 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
             return nullptr;
         }
     }
+    // B's rows not 16-byte multiples (N) while A's are (K): the TMA kernel,
+    // with B packed into aligned rows at run time, where the choice has one.
+    if (!tma_ok && !trans && !p->force_plain && !c.swap && (K * es) % 16 == 0)
+        p->tma = sat::find_entry(dt, c.bn, c.cg, sat::kProdTMA, c.stages);
     if (!trans) {
         p->plain = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlain);
         p->plain_strided = sat::find_entry(dt, c.bn < 128 ? 128 : c.bn, 1, sat::kProdPlainStrided);
@@ -325,7 +329,15 @@ gemm_plan* create(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, const cha
         if (p->cls)
             p->slots_cls = slots_for(p, p->cls);
 
-        p->ldb_pack = (N * es + 15) / 16 * 16 / es;
+        // Packed rows of B span an odd number of whole 128-byte lines: each
+        // TMA box row is then one line (rows only 16-byte aligned straddle
+        // two, and five 32-byte sectors), and rows do not repeat at a
+        // power-of-two stride. At bf16 (8191, 4097, 2049) the packed B read
+        // with 4104-element rows cost 16 us more than with 4160.
+        int64_t lines = (N * es + 127) / 128;
+        if (lines % 2 == 0)
+            ++lines;
+        p->ldb_pack = lines * 128 / es;
     }
     for (const sat::KernelEntry* k : {p->tma, p->plain, p->plain_strided, p->cls}) {
         if (!k)
@@ -536,10 +548,12 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
     const int64_t es64 = static_cast<int64_t>(es);
     const bool a_rows_ok = reinterpret_cast<uintptr_t>(A) % 16 == 0 && (lda * es64) % 16 == 0;
     const bool b_rows_ok = reinterpret_cast<uintptr_t>(B) % 16 == 0 && (ldb * es64) % 16 == 0;
-    const bool use_tma = p->tma && a_rows_ok && b_rows_ok;
+    // B's rows, where TMA cannot address them, are packed into this
+    // stream's aligned copy first (untransposed B only).
+    const bool b_pack_ok = !p->trans_b && p->ldb_pack > 0;
+    const bool use_tma = p->tma && a_rows_ok && (b_rows_ok || b_pack_ok);
     // Otherwise (untransposed plans) the class-view kernel: A through one
-    // tensor map per residue class of row index, B as it lies when its rows
-    // are aligned, else packed into this stream's aligned copy.
+    // tensor map per residue class of row index, B as it lies or packed.
     const bool use_cls = !use_tma && p->cls != nullptr;
     if (!use_tma && !use_cls && !p->plain)
         return fail(GEMM_ERR_ALIGN,
@@ -641,9 +655,9 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         !sat::sk_layout(tiles_m * tiles_n, a.num_kb, p->slots_cls, &sk_tiles, &sk_w))
         sk_tiles = sk_w = 0;
     const bool sk = sk_tiles > 0;
-    const bool pack = use_cls && !b_rows_ok;
-    // Split-K and stream-K runs, and class-view runs whose B must be packed,
-    // write this stream's scratch set, held (with the plan's scratch lock)
+    const bool pack = (use_tma || use_cls) && !b_rows_ok;
+    // Split-K and stream-K runs, and runs whose B must be packed, write this
+    // stream's scratch set, held (with the plan's scratch lock)
     // until the run is enqueued and its end recorded.
     std::unique_lock<std::mutex> slock(p->scratch_mu, std::defer_lock);
     Scratch* sc = nullptr;
@@ -723,19 +737,19 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         }
         tmC = p->tmC;
     }
+    // B as it lies, or packed into rows of ldb_pack elements (whole 128-byte
+    // lines) first, on the same stream.
+    const void* bsrc = B;
+    int64_t bld = ldb;
+    if (pack) {
+        e = sat::launch_pack_rows(B, ldb * es64, sc->bpack, p->ldb_pack * es64, p->K, p->N * es64, p->sm_count,
+                                  stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launching the packing of B");
+        bsrc = sc->bpack;
+        bld = p->ldb_pack;
+    }
     if (use_cls) {
-        // B as it lies, or packed into rows of ldb_pack elements (16-byte
-        // multiples) first, on the same stream.
-        const void* bsrc = B;
-        int64_t bld = ldb;
-        if (pack) {
-            e = sat::launch_pack_rows(B, ldb * es64, sc->bpack, p->ldb_pack * es64, p->K, p->N * es64, p->sm_count,
-                                      stream);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "launching the packing of B");
-            bsrc = sc->bpack;
-            bld = p->ldb_pack;
-        }
         std::lock_guard<std::mutex> lock(p->mu);
         if (p->cls_B != bsrc || p->cls_ldb != bld) {
             const int rc = encode_2d(&p->tmClsB, p->dt, bsrc, p->N, p->K, static_cast<uint32_t>(128 / es),
@@ -770,16 +784,16 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
             p->map_A = A;
             p->map_lda = lda;
         }
-        if (p->map_B != B || p->map_ldb != ldb) {
-            const int rc = p->trans_b ? encode_2d(&p->tmB, p->dt, B, p->K, p->N, bk,
-                                                  static_cast<uint32_t>(k->bn / k->cg), CU_TENSOR_MAP_SWIZZLE_128B, ldb)
-                                      : encode_2d(&p->tmB, p->dt, B, p->N, p->K, cw, bk, mn_swz, ldb);
+        if (p->map_B != bsrc || p->map_ldb != bld) {
+            const int rc = p->trans_b ? encode_2d(&p->tmB, p->dt, bsrc, p->K, p->N, bk,
+                                                  static_cast<uint32_t>(k->bn / k->cg), CU_TENSOR_MAP_SWIZZLE_128B, bld)
+                                      : encode_2d(&p->tmB, p->dt, bsrc, p->N, p->K, cw, bk, mn_swz, bld);
             if (rc) {
                 p->map_B = nullptr;
                 return rc;
             }
-            p->map_B = B;
-            p->map_ldb = ldb;
+            p->map_B = bsrc;
+            p->map_ldb = bld;
         }
         tmA = p->tmA;
         tmB = p->tmB;

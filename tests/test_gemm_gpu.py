@@ -302,6 +302,24 @@ def test_class_view_rows_dyadic_exact(dtype, config):
         checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
 
 
+# N not a 16-byte multiple while K is: A's rows are TMA-addressable, B's
+# are not. The TMA kernel reads B from the stream's packed copy (rows of
+# whole 128-byte lines); C's misaligned rows take the row-store epilogue.
+@pytest.mark.parametrize("config", [None, "256,2,0,4", "128,1,1,2", "256,1,0,8,2", "256,2,1,4,sk"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16", "fp16"])
+def test_tma_kernel_with_b_rows_packed(dtype, config):
+    for i, (M, N, K) in enumerate([(1000, 517, 256), (300, 3001, 512), (2600, 2049, 320)]):
+        A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 90 + i, "dyadic")
+        _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+        got, desc = run_np(M, N, K, dtype, A, B, C0, 1.5, 0.5, config)
+        assert " tma " in desc, desc
+        checks.assert_bit_exact(got, ref32, f"{dtype} {M}x{N}x{K} [{desc}]")
+    A, B, C0 = si.problem(2600, 2049, 320, dtype, "normal", 93, "normal")
+    ref64, _ = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    got, desc = run_np(2600, 2049, 320, dtype, A, B, C0, 1.5, 0.5, config)
+    checks.assert_rel_rms(got, ref64, si.REL_RMS_BOUND[dtype], f"{dtype} gaussian [{desc}]")
+
+
 @pytest.mark.parametrize("config", ["128,1,0,4,plain", "256,1,1,2,plain", "128,1,0,4", "256,2,1,2",
                                     "256,2,0,4,fwd", "128,1,0,4,2"])
 @pytest.mark.parametrize("dtype", ["tf32", "bf16"])
