@@ -799,6 +799,16 @@ int run_impl(const gemm_plan* p, const void* A, int64_t lda, const void* B, int6
         tmB = p->tmB;
     }
     if (use_cls) {
+        // Class-view tiles write fp32 C rows in 16-byte stores when the rows P
+        // apart lie a whole number of 16-byte units apart (unsplit runs
+        // without stream-K pieces): rows that start 16-byte aligned always;
+        // the others, whose ends take element-wise stores, only where the
+        // epilogue is the slower stage, i.e. 16-bit operands (half the MMA
+        // time per tile of TF32) with C read as well as written. Measured at
+        // (8191, 4097, 2049): bf16 beta 0.5 158 -> 150 us; bf16 beta 0 130 ->
+        // 140 us and tf32 beta 0.5 228 -> 240 us, where they are not used.
+        if (!split && !sk && p->c_half == 0 && (static_cast<int64_t>(a.a_classes) * ldc) % 4 == 0)
+            a.c_cls = p->dt != sat::kDtTF32 && beta != 0.0f ? 2 : 1;
         // Class maps are copied under the lock: another thread may re-encode them.
         CUtensorMap cmaps[sat::kMaxClasses];
         {

@@ -65,6 +65,11 @@ struct GemmArgs {
     int a_classes;
     int a_rows[kMaxClasses];
     int a_shift[kMaxClasses];
+    // Class-view tiles, fp32 C whose rows P apart lie a whole number of
+    // 16-byte units apart (so all rows of a tile share one offset): the
+    // epilogue stores the 16-byte-aligned part of each row in 16-byte units,
+    // for rows that start on a 16-byte boundary (1) or for every row (2).
+    int c_cls;
     uint32_t* err;             // device error word (bounded-wait timeouts), may be null
     unsigned long long timeout_ns;
 };

@@ -262,6 +262,11 @@ __device__ __forceinline__ uint32_t swz_mnmajor(int k, int n)
            ((((nb >> 4) ^ static_cast<uint32_t>(k & 7)) << 4) | (nb & 15u));
 }
 
+// One A tensor map per residue class of row index (class-view A).
+struct ClassMaps {
+    CUtensorMap a[kMaxClasses];
+};
+
 // The GEMM of `args`, as a device routine: the part of the persistent tile
 // schedule that falls to this CTA (CTAs blockIdx.x of gridDim.x, in pairs for
 // CG == 2). Any kernel can call it once, with all of its threads, as one phase
@@ -329,6 +334,8 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
     // Class-view tiles hold rows P apart: their C goes out by rows, never as
     // bulk-store boxes.
     const int c_tma = T::CLS ? 0 : args.c_tma;
+    // Class-view tiles whose C rows all share one 16-byte offset (c_cls).
+    const bool c_cls = T::CLS && args.c_cls != 0;
     const bool c_ring = T::C_RING_OK && args.c_ring != 0 && c_tma != 0 && args.splits == 1 && args.sk_tiles == 0 &&
                         args.beta != 0.0f;
 
@@ -877,6 +884,9 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
         const float alpha = args.alpha, beta = args.beta;
         const int ldc = args.ldc;
         constexpr int NCHUNK = BN / 32;
+        // C's element address (fp32): row r starts (c_el + r * ldc) mod 4
+        // elements past a 16-byte boundary.
+        const uint64_t c_el = reinterpret_cast<uintptr_t>(args.C) >> 2;
         // C values (bulk-store path, beta != 0) of row (row0 + lane), columns
         // gcol0 .. gcol0 + 31, as 8 aligned float4 loads; zero outside M x N.
         auto load_c = [&](float (&cv)[32], int grow, int gcol0) {
@@ -1182,6 +1192,69 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap* tmA, const CUtensorM
                         }
                     }
                     __syncwarp();
+                    // This class's rows start s elements past a 16-byte boundary.
+                    const int s = T::CLS ? static_cast<int>((c_el + static_cast<uint64_t>(cls + ncls * row0) * ldc) & 3u)
+                                         : 0;
+                    if constexpr (T::CLS && MODE == 0) {
+                        if (c_cls && gcol0 + 32 <= args.N && (s == 0 || args.c_cls == 2)) {
+                            // Class-view tiles, fp32 C whose rows P apart lie a
+                            // whole number of 16-byte units apart: every row of
+                            // the chunk starts s elements past a 16-byte boundary.
+                            // Columns lo .. lo + w - 1 of each row (lo = (4 - s) %
+                            // 4, w = 32 or 28) leave in 16-byte stores, lanes on
+                            // consecutive 16-byte units; the other 4 - s + s
+                            // columns (at the chunk's two ends, in 16-byte units
+                            // shared with the neighbouring chunks) go element by
+                            // element, one row per lane. A chunk that reaches
+                            // past column N, and (c_cls == 1) misaligned rows,
+                            // take the row stores below.
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                v[i] = alpha * buf[i * 32 + (lane ^ i)];
+                                if (beta != 0.0f)
+                                    v[i] = fmaf(beta, cv[i], v[i]);
+                            }
+                            __syncwarp();
+                            const int lo = s ? 4 - s : 0, w = s ? 28 : 32;
+                            // Stage: columns lo .. lo + w - 1 as rows of w floats,
+                            // then the 4 edge columns (the first lo, the last s).
+                            const int bc = lane - lo;
+                            if (bc >= 0 && bc < w) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    buf[i * w + bc] = v[i];
+                            } else {
+                                const int e = lane < lo ? lane : lane - w;
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    buf[32 * 28 + i * 4 + e] = v[i];
+                            }
+                            __syncwarp();
+                            // 16-byte unit u = t * 32 + lane of the w / 4 per row.
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) {
+                                const int u = t * 32 + lane;
+                                const int row = s ? u / 7 : u >> 3;
+                                const int g = u - row * (w >> 2);
+                                if (row < min(nrows, 32)) {
+                                    float x0, x1, x2, x3;
+                                    ld_shared_v4(sb + static_cast<uint32_t>(u * 16), x0, x1, x2, x3);
+                                    st_global_v4(args.C + static_cast<int64_t>(cls + ncls * (row0 + row)) * ldc + gcol0 + lo +
+                                                     4 * g,
+                                                 x0, x1, x2, x3);
+                                }
+                            }
+                            if (s != 0 && lane < nrows) {
+                                const int64_t e0 = static_cast<int64_t>(cls + ncls * (row0 + lane)) * ldc + gcol0;
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    args.C[e0 + (e < lo ? e : e + 28)] = buf[32 * 28 + lane * 4 + e];
+                            }
+                            __syncwarp();
+                            continue;
+                        }
+                    }
                     if (col < args.N) {
                         const int kind = args.c_half;
 #pragma unroll
@@ -1254,11 +1327,6 @@ __global__ void __launch_bounds__(Traits<DT, BN, CG, PROD, ST>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     gemm_cta<DT, BN, CG, PROD, ST>(&tmA, tmB, tmC, args, smem_raw);
 }
-
-// One A tensor map per residue class of row index (class-view A).
-struct ClassMaps {
-    CUtensorMap a[kMaxClasses];
-};
 
 template <int DT, int BN, int CG, int ST>
 __global__ void __launch_bounds__(Traits<DT, BN, CG, kProdClassA, ST>::THREADS, 1)

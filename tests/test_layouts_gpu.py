@@ -177,3 +177,36 @@ def test_16_bit_c_with_k_zero_scales_in_place():
         plan.run(0, 0, dC, 1.0, 0.5, stream())
         torch.cuda.synchronize()
     assert np.array_equal(dC.cpu().numpy(), _c16(0.5 * C0, "bf16"))
+
+
+# Class-view tiles write fp32 C rows in 16-byte stores when the rows P apart
+# lie a whole number of 16-byte units apart: each chunk's 16-byte-aligned
+# columns as whole units, and the columns at the chunk's two ends (sharing
+# 16-byte units with the neighbouring chunks) element by element.
+# C sits coff floats into its allocation with row stride N + dldc; every
+# float around it holds a sentinel that must survive. K = 131 gives P = 4
+# (tf32) or 8 (bf16), where every ldc qualifies; K = 130 (tf32) and 132
+# (bf16) give P = 2, where odd ldc keeps the element-wise row stores.
+@pytest.mark.parametrize("K", [131, 130, 132])
+@pytest.mark.parametrize("coff", [0, 3])
+@pytest.mark.parametrize("dldc", [0, 1, 3])
+@pytest.mark.parametrize("config", [None, "128,1,0,4", "256,1,1,2"])
+@pytest.mark.parametrize("dtype", ["tf32", "bf16"])
+def test_class_view_c_boxes_and_edge_columns(dtype, config, dldc, coff, K):
+    M, N = 700, 600
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 95, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, dtype)
+    ldc = N + dldc
+    Cs = np.full(coff + M * ldc + 8, SENTINEL, np.float32)
+    Cs[coff:coff + M * ldc].reshape(M, ldc)[:, :N] = C0
+    dC = to_dev(Cs)
+    with sat.Plan(M, N, K, dtype, config) as plan:
+        desc = plan.describe()
+        plan.run(to_dev(A, dtype), to_dev(B, dtype), dC.data_ptr() + 4 * coff, 1.5, 0.5, stream(), ldc=ldc)
+        torch.cuda.synchronize()
+        sat.check(plan.status())
+    out = dC.cpu().numpy()
+    view = out[coff:coff + M * ldc].reshape(M, ldc)
+    assert np.all(out[:coff] == SENTINEL) and np.all(out[coff + M * ldc:] == SENTINEL), f"outside C [{desc}]"
+    assert np.all(view[:, N:] == SENTINEL), f"C padding was written [{desc}]"
+    checks.assert_bit_exact(view[:, :N], ref32, f"{dtype} K {K} ldc {ldc} offset {coff} [{desc}]")
