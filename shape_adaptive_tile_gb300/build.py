@@ -22,14 +22,16 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libsatgemm.so")
 STAMP = os.path.join(LIB_DIR, "libsatgemm.stamp")
 
-SOURCES = ["api.cu", "aux_kernels.cu", "dispatch.cpp", "tensor_map.cpp", "kernels_tf32.cu", "kernels_bf16.cu",
-           "kernels_fp16.cu", "noalloc.cu", "device_call.cu", "rowops.cu"]
+# The kernel variants come as three translation units per dtype (they take
+# most of the build); the longest units are listed first.
+SOURCES = [f"kernels_{dt}{grp}.cu" for grp in ("", "_alt", "_trans") for dt in ("tf32", "bf16", "fp16")] + [
+    "device_call.cu", "api.cu", "aux_kernels.cu", "dispatch.cpp", "tensor_map.cpp", "noalloc.cu", "rowops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 # The GEMM kernel units: an explicit register ceiling (the launch bounds of
 # a 320-thread, one-CTA-per-SM kernel allow 200) keeps ptxas from spilling
 # the epilogue at its own default of 168 registers.
-EXTRA = {f: ["-maxrregcount=200"] for f in ("kernels_tf32.cu", "kernels_bf16.cu", "kernels_fp16.cu", "device_call.cu")}
+EXTRA = {f: ["-maxrregcount=200"] for f in SOURCES if f.startswith("kernels_") or f == "device_call.cu"}
 
 
 def _nvcc() -> str:

@@ -186,16 +186,29 @@ cudaError_t launch_wait_probe(uint32_t* err, unsigned long long timeout_ns, cuda
 
 const KernelEntry* find_entry(int dt, int bn, int cg, int prod, int stages)
 {
-    const KernelEntry* tab = dt == kDtTF32 ? kEntriesTF32 : dt == kDtBF16 ? kEntriesBF16 : kEntriesFP16;
-    const int n = dt == kDtTF32 ? kNumEntriesTF32 : dt == kDtBF16 ? kNumEntriesBF16 : kNumEntriesFP16;
+    const KernelEntry* tab[3];
+    int num[3];
+    if (dt == kDtTF32) {
+        tab[0] = kEntriesTF32, tab[1] = kEntriesTF32Alt, tab[2] = kEntriesTF32Trans;
+        num[0] = kNumEntriesTF32, num[1] = kNumEntriesTF32Alt, num[2] = kNumEntriesTF32Trans;
+    } else if (dt == kDtBF16) {
+        tab[0] = kEntriesBF16, tab[1] = kEntriesBF16Alt, tab[2] = kEntriesBF16Trans;
+        num[0] = kNumEntriesBF16, num[1] = kNumEntriesBF16Alt, num[2] = kNumEntriesBF16Trans;
+    } else {
+        tab[0] = kEntriesFP16, tab[1] = kEntriesFP16Alt, tab[2] = kEntriesFP16Trans;
+        num[0] = kNumEntriesFP16, num[1] = kNumEntriesFP16Alt, num[2] = kNumEntriesFP16Trans;
+    }
     const KernelEntry* best = nullptr;
-    for (int i = 0; i < n; ++i) {
-        if (tab[i].bn != bn || tab[i].cg != cg || tab[i].prod != prod)
-            continue;
-        if (stages > 0 && tab[i].stages == stages)
-            return &tab[i];
-        if (stages == 0 && (!best || tab[i].stages > best->stages))
-            best = &tab[i];
+    for (int g = 0; g < 3; ++g) {
+        for (int i = 0; i < num[g]; ++i) {
+            const KernelEntry& k = tab[g][i];
+            if (k.bn != bn || k.cg != cg || k.prod != prod)
+                continue;
+            if (stages > 0 && k.stages == stages)
+                return &k;
+            if (stages == 0 && (!best || k.stages > best->stages))
+                best = &k;
+        }
     }
     return best;
 }

@@ -104,25 +104,29 @@ constexpr KernelEntry make_entry()
                        &launch_variant<DT, BN, CG, PROD, ST>};
 }
 
-// The variants compiled for every dtype.
-// The untransposed TMA tiles come with two ring depths each: the most
-// stages that fit, and a shallower ring (a dispatcher dimension, measured by
-// the sweep).
-#define SAT_ENTRIES(DT)                                                                                         \
+// The variants compiled for every dtype, in three groups (one translation
+// unit each, so that they compile in parallel).
+// Untransposed TMA tiles, with two ring depths each: the most stages that
+// fit, and a shallower ring (a dispatcher dimension, measured by the sweep).
+#define SAT_ENTRIES_TMA(DT)                                                                                     \
     make_entry<DT, 64, 1, kProdTMA, 0>(), make_entry<DT, 128, 1, kProdTMA, 0>(),                                \
         make_entry<DT, 256, 1, kProdTMA, 0>(), make_entry<DT, 128, 2, kProdTMA, 0>(),                           \
         make_entry<DT, 256, 2, kProdTMA, 0>(), make_entry<DT, 64, 1, kProdTMA, 4>(),                            \
         make_entry<DT, 128, 1, kProdTMA, 4>(), make_entry<DT, 256, 1, kProdTMA, 3>(),                           \
-        make_entry<DT, 128, 2, kProdTMA, 4>(), make_entry<DT, 256, 2, kProdTMA, 4>(),                           \
-        make_entry<DT, 128, 1, kProdPlain, 0>(), make_entry<DT, 256, 1, kProdPlain, 0>(),                       \
+        make_entry<DT, 128, 2, kProdTMA, 4>(), make_entry<DT, 256, 2, kProdTMA, 4>()
+// Plain loads, swapped operands and class views of A.
+#define SAT_ENTRIES_ALT(DT)                                                                                     \
+    make_entry<DT, 128, 1, kProdPlain, 0>(), make_entry<DT, 256, 1, kProdPlain, 0>(),                           \
         make_entry<DT, 128, 1, kProdPlainStrided, 0>(), make_entry<DT, 256, 1, kProdPlainStrided, 0>(),         \
         make_entry<DT, 32, 1, kProdSwap, 0>(), make_entry<DT, 64, 1, kProdSwap, 0>(),                           \
-        make_entry<DT, 128, 1, kProdSwap, 0>(), make_entry<DT, 128, 1, kProdTN, 0>(),                           \
-        make_entry<DT, 256, 1, kProdTN, 0>(), make_entry<DT, 256, 2, kProdTN, 0>(),                             \
-        make_entry<DT, 128, 1, kProdNT, 0>(), make_entry<DT, 256, 1, kProdNT, 0>(),                             \
-        make_entry<DT, 256, 2, kProdNT, 0>(), make_entry<DT, 128, 1, kProdTT, 0>(),                             \
-        make_entry<DT, 256, 1, kProdTT, 0>(), make_entry<DT, 256, 2, kProdTT, 0>(),                             \
-        make_entry<DT, 128, 1, kProdClassA, 0>(), make_entry<DT, 256, 1, kProdClassA, 0>(),                     \
-        make_entry<DT, 256, 2, kProdClassA, 0>()
+        make_entry<DT, 128, 1, kProdSwap, 0>(), make_entry<DT, 128, 1, kProdClassA, 0>(),                       \
+        make_entry<DT, 256, 1, kProdClassA, 0>(), make_entry<DT, 256, 2, kProdClassA, 0>()
+// Transposed operands.
+#define SAT_ENTRIES_TRANS(DT)                                                                                   \
+    make_entry<DT, 128, 1, kProdTN, 0>(), make_entry<DT, 256, 1, kProdTN, 0>(),                                 \
+        make_entry<DT, 256, 2, kProdTN, 0>(), make_entry<DT, 128, 1, kProdNT, 0>(),                             \
+        make_entry<DT, 256, 1, kProdNT, 0>(), make_entry<DT, 256, 2, kProdNT, 0>(),                             \
+        make_entry<DT, 128, 1, kProdTT, 0>(), make_entry<DT, 256, 1, kProdTT, 0>(),                             \
+        make_entry<DT, 256, 2, kProdTT, 0>()
 
 }  // namespace sat

@@ -28,13 +28,13 @@ struct KernelEntry {
                           const GemmArgs* args, int grid, cudaStream_t stream);
 };
 
-// Defined in kernels_<dtype>.cu.
-extern const KernelEntry kEntriesTF32[];
-extern const int kNumEntriesTF32;
-extern const KernelEntry kEntriesBF16[];
-extern const int kNumEntriesBF16;
-extern const KernelEntry kEntriesFP16[];
-extern const int kNumEntriesFP16;
+// Defined in kernels_<dtype>.cu, kernels_<dtype>_alt.cu and kernels_<dtype>_trans.cu.
+extern const KernelEntry kEntriesTF32[], kEntriesTF32Alt[], kEntriesTF32Trans[];
+extern const int kNumEntriesTF32, kNumEntriesTF32Alt, kNumEntriesTF32Trans;
+extern const KernelEntry kEntriesBF16[], kEntriesBF16Alt[], kEntriesBF16Trans[];
+extern const int kNumEntriesBF16, kNumEntriesBF16Alt, kNumEntriesBF16Trans;
+extern const KernelEntry kEntriesFP16[], kEntriesFP16Alt[], kEntriesFP16Trans[];
+extern const int kNumEntriesFP16, kNumEntriesFP16Alt, kNumEntriesFP16Trans;
 
 // Sets the message gemm_last_error() returns on this thread (api.cu).
 void set_last_error(const char* msg);
