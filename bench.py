@@ -78,6 +78,17 @@ def tensor_peak(dtype, pk, sustained=False):
     return pk[key] * NOMINAL_TFLOPS[dtype] / NOMINAL_TFLOPS["bf16"]
 
 
+def roofline_peak(dtype, pk, clocks):
+    """(peak, burst peak, "burst" or "sustained") for a contraction of
+    `dtype`: the sustained figure when the clock samples taken inside the
+    timed region show the power cap, else the burst one."""
+    clk = clocks or {}
+    capped = "sw_power_cap" in (clk.get("reasons") or []) and (clk.get("samples_in_timed_region") or 0) > 0
+    burst = tensor_peak(dtype, pk)
+    peak = tensor_peak(dtype, pk, sustained=capped)
+    return peak, burst, "sustained" if peak != burst else "burst"
+
+
 def min_bytes(dtype, M, N, K, beta):
     es = 4 if dtype == "tf32" else 2
     return es * (M * K + K * N) + 4 * M * N * (2 if beta != 0 else 1)
@@ -512,10 +523,7 @@ def main():
     # back-to-back steps of a long run settle there, as the sustained
     # measurement did).
     clk = r["clocks"] or {}
-    capped = "sw_power_cap" in (clk.get("reasons") or []) and (clk.get("samples_in_timed_region") or 0) > 0
-    burst = tensor_peak(r["dtype"], pk)
-    peak = tensor_peak(r["dtype"], pk, sustained=capped)
-    kind = "sustained" if peak != burst else "burst"
+    peak, burst, kind = roofline_peak(r["dtype"], pk, clk)
     achieved = r["flops"] / (ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

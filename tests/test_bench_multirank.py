@@ -58,3 +58,23 @@ def test_reference_arm_non_zero_rank_exits_quietly():
                         "--steps", "3", "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_roofline_peak_follows_the_clock_record():
+    # The measured bf16 figures times the nominal TF32 : BF16 ratio; the
+    # sustained one only when the timed region's clock samples show the
+    # power cap.
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"bf16_tflops": 1892.0, "bf16_tflops_sustained": 1684.0}
+    capped = {"reasons": ["sw_power_cap"], "samples_in_timed_region": 12}
+    peak, burst, kind = bench.roofline_peak("tf32", pk, capped)
+    assert (kind, round(peak, 3), round(burst, 3)) == ("sustained", round(1684.0 * 1100 / 2250, 3),
+                                                      round(1892.0 * 1100 / 2250, 3))
+    for clocks in ({"reasons": [], "samples_in_timed_region": 12}, {"reasons": ["sw_power_cap"],
+                                                                     "samples_in_timed_region": 0}, None):
+        peak, burst, kind = bench.roofline_peak("bf16", pk, clocks)
+        assert kind == "burst" and peak == burst == 1892.0
+    # No sustained figure recorded: the burst one either way.
+    peak, _, kind = bench.roofline_peak("fp16", {"bf16_tflops": 1900.0}, capped)
+    assert kind == "burst" and peak == 1900.0
