@@ -138,3 +138,45 @@ def test_rowop_special_values_and_errors():
     assert sat.rowop_softmax(dx, 4, dx, 8, 4, 8, stream()) == -1          # stride below width
     assert sat.rowop_softmax(None, 8, dx, 8, 4, 8, stream()) == -1
     assert sat.rowop_rmsnorm(dx, 40000, None, dx, 40000, 1, 32769, 1e-5, stream()) == -1   # too wide
+
+
+@pytest.mark.parametrize("i", range(60))
+def test_random_rows_strides_and_offsets(i):
+    # Seeded random rows x width, row strides (ldx, ldy >= width) and float
+    # offsets of X and Y (16-byte loads only where everything allows them),
+    # gamma and beta present or not; every output against the oracle, and the
+    # padding around Y untouched.
+    rng = np.random.default_rng(7000 + i)
+    op = si.ROWOPS[i % 3]
+    rows = int(rng.integers(1, 300))
+    width = int(rng.integers(1, 20000)) if i % 4 else int(rng.integers(1, 600))
+    ldx, ldy = width + int(rng.integers(0, 9)), width + int(rng.integers(0, 9))
+    ox, oy = int(rng.integers(0, 4)), int(rng.integers(0, 4))
+    x, g, b = si.rowop_inputs(rows, width, seed=40 + i)
+    if rng.integers(0, 2):
+        g = None
+    if rng.integers(0, 2):
+        b = None
+    fx = np.zeros(ox + rows * ldx + 4, np.float32)
+    fx[ox:ox + rows * ldx].reshape(rows, ldx)[:, :width] = x
+    fy = np.full(oy + rows * ldy + 4, -777.0, np.float32)
+    dx, dy = torch.from_numpy(fx).cuda(), torch.from_numpy(fy).cuda()
+    dg = torch.from_numpy(g).cuda() if g is not None else None
+    db = torch.from_numpy(b).cuda() if b is not None else None
+    px, py = dx.data_ptr() + 4 * ox, dy.data_ptr() + 4 * oy
+    if op == "softmax":
+        rc = sat.rowop_softmax(px, ldx, py, ldy, rows, width, stream())
+    elif op == "rmsnorm":
+        rc = sat.rowop_rmsnorm(px, ldx, dg, py, ldy, rows, width, 1e-5, stream())
+    else:
+        rc = sat.rowop_layernorm(px, ldx, dg, db, py, ldy, rows, width, 1e-5, stream())
+    assert rc == 0, sat.gemm_last_error()
+    torch.cuda.synchronize()
+    out = dy.cpu().numpy()
+    view = out[oy:oy + rows * ldy].reshape(rows, ldy)
+    what = f"{op} rows={rows} width={width} ldx={ldx} ldy={ldy} offsets={ox},{oy} gamma={g is not None} beta={b is not None}"
+    assert np.all(out[:oy] == -777.0) and np.all(out[oy + rows * ldy:] == -777.0), f"outside Y: {what}"
+    assert np.all(view[:, width:] == -777.0), f"Y padding written: {what}"
+    ref = oracle.softmax(x) if op == "softmax" else oracle.rmsnorm(x, g) if op == "rmsnorm" else \
+        oracle.layernorm(x, g, b)
+    _check(op, view[:, :width], ref, what)
