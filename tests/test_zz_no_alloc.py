@@ -126,3 +126,29 @@ def test_noalloc_argument_errors():
     assert sat.gemm_run_noalloc(4, 4, 4, "tf32", x, x, None, 1.0, 0.0, stream()) == -1
     assert sat.gemm_run_noalloc(4, 4, 4, "tf32", x, x, x.data_ptr() + 2, 1.0, 0.0, stream()) == -3
     assert sat.gemm_run_noalloc(0, 4, 4, "tf32", None, None, None, 1.0, 0.0, stream()) == 0
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_noalloc_random_problems_bit_exact(i):
+    # Seeded random shapes and operand offsets (dense strides), dyadic inputs:
+    # the oracle's bits, twice in a row from the same fixed scratch.
+    rng = np.random.default_rng(4000 + i)
+    dtype = ("tf32", "bf16", "fp16")[i % 3]
+    M = int(rng.integers(1, 128)) if i % 5 == 4 else int(rng.integers(1, 2500))
+    N, K = int(rng.integers(1, 2500)), int(rng.integers(1, 3000))
+    alpha, beta = float(rng.choice([1.0, 1.5])), float(rng.choice([0.0, 0.5]))
+    off = int(rng.integers(0, 2))
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 600 + i, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, alpha, beta, dtype)
+    es = 4 if dtype == "tf32" else 2
+    fa = np.concatenate([np.zeros(off, A.dtype), A.ravel()])
+    fb = np.concatenate([np.zeros(off, B.dtype), B.ravel()])
+    dA, dB = to_dev(fa, dtype), to_dev(fb, dtype)
+    for call in range(2):
+        out = to_dev(C0)
+        rc = sat.gemm_run_noalloc(M, N, K, dtype, dA.data_ptr() + es * off, dB.data_ptr() + es * off, out, alpha,
+                                  beta, stream())
+        assert rc == 0, sat.gemm_last_error()
+        torch.cuda.synchronize()
+        checks.assert_bit_exact(out.cpu().numpy(), ref32,
+                                f"noalloc call {call + 1}: {dtype} {M}x{N}x{K} offset {off} alpha {alpha} beta {beta}")
