@@ -170,11 +170,17 @@ int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B
 
 /*
  * End-to-end form of gemm_run for operands in HOST memory (pinned host
- * memory gives asynchronous copies): on `cuda_stream`, copy hA -> dA,
- * hB -> dB and (only if beta != 0) hC -> dC, run the GEMM on the device
- * buffers, then copy dC -> hC. dA, dB, dC are caller-owned device buffers
- * of the full operand sizes. Returns after enqueueing; synchronise the
- * stream before reading hC.
+ * memory gives asynchronous copies): copy hA -> dA, hB -> dB and (only if
+ * beta != 0) hC -> dC, run the GEMM on the device buffers, then copy
+ * dC -> hC, all ordered on `cuda_stream` (after its earlier work, before its
+ * later work). dA, dB, dC are caller-owned device buffers of the full
+ * operand sizes. Large untransposed plans with fp32 C (M >= 1024 and at least
+ * 32 MiB of A and B) run in up to 4 row blocks whose copies overlap the
+ * GEMMs: the copies go on two streams of the calling stream's own (made by
+ * the plan's first such run on it), the blocks' GEMMs on `cuda_stream`
+ * through plans of the block's shape (made by the first such run and kept
+ * with the plan; gemm_plan_status reports their bounded-wait timeouts too).
+ * Returns after enqueueing; synchronise the stream before reading hC.
  */
 int gemm_run_host(const gemm_plan* plan, const void* hA, const void* hB, float* hC, float alpha, float beta,
                   void* dA, void* dB, float* dC, void* cuda_stream);

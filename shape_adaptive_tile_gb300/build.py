@@ -10,6 +10,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 
@@ -47,12 +48,25 @@ def _inputs():
     return [f for f in files if os.path.isfile(f)]
 
 
+# A C/C++ comment or a string or character literal (kept whole, so that a
+# comment marker inside a literal is not taken for a comment).
+_TOKEN = re.compile(rb'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def _code_text(data: bytes) -> bytes:
+    """The source with comments removed and runs of whitespace collapsed: a
+    profile stays valid across edits that change neither."""
+    data = _TOKEN.sub(lambda m: b" " if m.group(0)[:1] == b"/" else m.group(0), data)
+    return b" ".join(data.split())
+
+
 def source_hash() -> str:
-    """SHA-256 of the kernel and ABI sources (what a profile was taken of)."""
+    """SHA-256 of the kernel and ABI sources (what a profile was taken of),
+    comments and layout aside."""
     h = hashlib.sha256()
     for f in _inputs():
         with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+            h.update(os.path.basename(f).encode() + b"\0" + _code_text(fh.read()))
     return h.hexdigest()[:16]
 
 
@@ -62,14 +76,14 @@ _ROWOP_ONLY = ("rowops.cu", "rowops.h")
 
 def gemm_source_hash() -> str:
     """SHA-256 of the sources the GEMM kernels are built from: every input but
-    the row operators' own files. A profile of a GEMM kernel stays valid as
-    long as this is unchanged."""
+    the row operators' own files, comments and layout aside. A profile of a
+    GEMM kernel stays valid as long as this is unchanged."""
     h = hashlib.sha256()
     for f in _inputs():
         if os.path.basename(f) in _ROWOP_ONLY:
             continue
         with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+            h.update(os.path.basename(f).encode() + b"\0" + _code_text(fh.read()))
     return h.hexdigest()[:16]
 
 

@@ -95,8 +95,14 @@ struct Scratch {
     void* bpack = nullptr;             // B in rows of whole 128-byte lines (K x ldb_pack elements), when its own rows are not TMA-addressable
     cudaEvent_t done = nullptr;        // recorded after each run that used this set
     unsigned long long last_use = 0;
+    // gemm_run_host in row blocks: copy streams (host to device, device to
+    // host) and their events (start, one per block copied in, one per block
+    // computed, end).
+    cudaStream_t cp_in = nullptr, cp_out = nullptr;
+    cudaEvent_t hev[2 + 2 * 4] = {};
 };
 constexpr int kMaxScratch = 8;
+constexpr int kHostBlocks = 4;  // row blocks of a pipelined gemm_run_host
 constexpr int kTicketPad = 32;  // the ticket counter sits 128 bytes past the last CTA counter
 
 }  // namespace
@@ -138,6 +144,10 @@ struct gemm_plan {
     unsigned long long timeout_ns = 2000000000ull;
     char desc[256] = "";
     mutable std::mutex mu;
+    // Plans for the row blocks of a pipelined gemm_run_host (rows of every
+    // block but the last, and of the last), made by its first such run.
+    mutable gemm_plan* host_plan[2] = {nullptr, nullptr};
+    mutable int64_t host_rows[2] = {0, 0};
     mutable const void* map_A = nullptr;
     mutable const void* map_B = nullptr;
     mutable const void* map_C = nullptr;
@@ -431,6 +441,12 @@ void free_scratch(Scratch& s)
             cudaFree(d);
     if (s.done)
         cudaEventDestroy(s.done);
+    for (cudaEvent_t ev : s.hev)
+        if (ev)
+            cudaEventDestroy(ev);
+    for (cudaStream_t st : {s.cp_in, s.cp_out})
+        if (st)
+            cudaStreamDestroy(st);
     s = Scratch{};
 }
 
@@ -867,6 +883,8 @@ void gemm_plan_destroy(gemm_plan* plan)
         return;
     for (int i = 0; i < plan->n_scratch; ++i)
         free_scratch(plan->scratch[i]);
+    for (gemm_plan* sub : plan->host_plan)
+        gemm_plan_destroy(sub);
     if (plan->h_err)
         cudaFreeHost(plan->h_err);
     delete plan;
@@ -902,12 +920,102 @@ int gemm_run_host(const gemm_plan* p, const void* hA, const void* hB, float* hC,
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const size_t es = static_cast<size_t>(elem_size(p->dt));
     cudaError_t e = cudaSuccess;
+    const size_t cbytes = static_cast<size_t>(p->M * p->N) * sizeof(float);
+    // Large untransposed fp32-C problems go in row blocks: B, then each block
+    // of A (and of C when beta != 0) copied in on a copy stream, each block's
+    // GEMM on `stream` as soon as its rows have arrived, and each block of C
+    // copied out on a second copy stream as soon as it is computed. The copies
+    // in, the GEMMs and the copies out then overlap.
+    const size_t in_bytes = static_cast<size_t>(p->M * p->K + p->K * p->N) * es;
+    if (p->K > 0 && alpha != 0.0f && !p->trans_a && !p->trans_b && p->c_half == 0 && p->M >= 1024 &&
+        in_bytes >= (size_t(32) << 20)) {
+        const int64_t blk = ((p->M + kHostBlocks - 1) / kHostBlocks + 255) / 256 * 256;
+        const int nb = static_cast<int>((p->M + blk - 1) / blk);
+        const int64_t last = p->M - (nb - 1) * blk;
+        gemm_plan* sub[2] = {nullptr, nullptr};
+        {
+            std::lock_guard<std::mutex> lock(p->mu);
+            for (int j = 0; j < 2; ++j) {
+                const int64_t rows = j == 0 ? blk : last;
+                if (!p->host_plan[j] || p->host_rows[j] != rows) {
+                    gemm_plan_destroy(p->host_plan[j]);
+                    p->host_plan[j] = create(rows, p->N, p->K, static_cast<gemm_dtype_t>(p->dt), nullptr);
+                    p->host_rows[j] = p->host_plan[j] ? rows : 0;
+                    if (!p->host_plan[j])
+                        return GEMM_ERR_LAUNCH;  // create() set the message
+                }
+                sub[j] = p->host_plan[j];
+            }
+        }
+        std::lock_guard<std::mutex> slock(p->scratch_mu);
+        Scratch* sc = nullptr;
+        int rc = acquire_scratch(p, s, false, &sc);
+        if (rc)
+            return rc;
+        if (!sc->cp_in) {
+            e = cudaStreamCreateWithFlags(&sc->cp_in, cudaStreamNonBlocking);
+            if (e == cudaSuccess)
+                e = cudaStreamCreateWithFlags(&sc->cp_out, cudaStreamNonBlocking);
+            for (cudaEvent_t& ev : sc->hev)
+                if (e == cudaSuccess)
+                    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "creating the copy streams of gemm_run_host");
+        }
+        cudaEvent_t ev_start = sc->hev[0], ev_end = sc->hev[1];
+        cudaEvent_t* ev_in = sc->hev + 2;
+        cudaEvent_t* ev_done = sc->hev + 2 + kHostBlocks;
+        const char* what = "enqueueing gemm_run_host's row blocks";
+        // Copies in wait for everything before this call on `stream`.
+        e = cudaEventRecord(ev_start, s);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(sc->cp_in, ev_start, 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(p->K * p->N) * es, cudaMemcpyHostToDevice, sc->cp_in);
+        for (int b = 0; b < nb && e == cudaSuccess; ++b) {
+            const int64_t r0 = b * blk, rows = b == nb - 1 ? last : blk;
+            e = cudaMemcpyAsync(static_cast<char*>(dA) + r0 * p->K * es, static_cast<const char*>(hA) + r0 * p->K * es,
+                                static_cast<size_t>(rows * p->K) * es, cudaMemcpyHostToDevice, sc->cp_in);
+            if (e == cudaSuccess && beta != 0.0f)
+                e = cudaMemcpyAsync(dC + r0 * p->N, hC + r0 * p->N, static_cast<size_t>(rows * p->N) * sizeof(float),
+                                    cudaMemcpyHostToDevice, sc->cp_in);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(ev_in[b], sc->cp_in);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(e, what);
+        for (int b = 0; b < nb; ++b) {
+            const int64_t r0 = b * blk;
+            e = cudaStreamWaitEvent(s, ev_in[b], 0);
+            if (e != cudaSuccess)
+                return cuda_fail(e, what);
+            rc = gemm_run(sub[b == nb - 1 ? 1 : 0], static_cast<const char*>(dA) + r0 * p->K * es, dB, dC + r0 * p->N,
+                          alpha, beta, cuda_stream);
+            if (rc)
+                return rc;
+            e = cudaEventRecord(ev_done[b], s);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(sc->cp_out, ev_done[b], 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(hC + r0 * p->N, dC + r0 * p->N,
+                                    static_cast<size_t>((b == nb - 1 ? last : blk) * p->N) * sizeof(float),
+                                    cudaMemcpyDeviceToHost, sc->cp_out);
+            if (e != cudaSuccess)
+                return cuda_fail(e, what);
+        }
+        // `stream` continues once the last block of C is on the host.
+        e = cudaEventRecord(ev_end, sc->cp_out);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(s, ev_end, 0);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(sc->done, s);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e, what);
+    }
     if (p->K > 0 && alpha != 0.0f) {
         e = cudaMemcpyAsync(dA, hA, static_cast<size_t>(p->M * p->K) * es, cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(dB, hB, static_cast<size_t>(p->K * p->N) * es, cudaMemcpyHostToDevice, s);
     }
-    const size_t cbytes = static_cast<size_t>(p->M * p->N) * sizeof(float);
     if (e == cudaSuccess && beta != 0.0f)
         e = cudaMemcpyAsync(dC, hC, cbytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess)
@@ -927,8 +1035,11 @@ int gemm_plan_status(const gemm_plan* p)
     if (e != cudaSuccess)
         return cuda_fail(e, "device error");
     volatile uint32_t* w = reinterpret_cast<volatile uint32_t*>(p->h_err);
-    const uint32_t h = *w;
+    uint32_t h = *w;
     *w = 0;
+    for (const gemm_plan* sub : p->host_plan)
+        if (sub && gemm_plan_status(sub) == GEMM_ERR_TIMEOUT)
+            h |= 1u << 31;  // a row block of gemm_run_host gave up a wait
     if (h) {
         // A launch that gave up may have left stream-K counters short of its
         // number: start the numbering again from cleared counters.

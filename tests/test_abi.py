@@ -169,6 +169,31 @@ def test_gemm_source_hash_ignores_only_the_row_operators(tmp_path, monkeypatch):
     assert b.gemm_source_hash() != h0
 
 
+def test_source_hash_ignores_comments_and_layout_only(tmp_path, monkeypatch):
+    # A profile stays valid across a comment edit, not across a code edit,
+    # and a comment marker inside a string literal is code.
+    import importlib
+    b = importlib.import_module("shape_adaptive_tile_gb300.build")
+    src = tmp_path / "csrc"
+    inc = tmp_path / "include"
+    src.mkdir()
+    inc.mkdir()
+    (inc / "gemm.h").write_text("int f(int);\n")
+    k = src / "gemm_kernel.cuh"
+    k.write_text('int f(int x) { return x + 1; }  // one\nconst char* s = "a//b";\n')
+    monkeypatch.setattr(b, "CSRC", str(src))
+    monkeypatch.setattr(b, "INCLUDE", str(inc))
+    h0 = b.gemm_source_hash()
+    k.write_text('/* new\n   block */ int f(int x)\n{\n  return x + 1;  // two\n}\nconst char* s = "a//b";\n')
+    assert b.gemm_source_hash() == h0
+    k.write_text('int f(int x) { return x + 2; }  // one\nconst char* s = "a//b";\n')
+    assert b.gemm_source_hash() != h0
+    k.write_text('int f(int x) { return x + 1; }  // one\nconst char* s = "a//c";\n')
+    assert b.gemm_source_hash() != h0
+    k.write_text("int f(int x) { return x + 1; }\nconst char* s = \"a//b\"; char c = '/';\n")
+    assert b.gemm_source_hash() != h0
+
+
 def test_noalloc_scratch_holds_every_dispatcher_choice_on_a_gb300():
     # gemm_run_noalloc keeps its partial tiles in a fixed array of 32 MiB
     # minus a 4 KiB status area (status word, then one stream-K counter per

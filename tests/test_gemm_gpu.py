@@ -441,6 +441,28 @@ def test_run_host_end_to_end():
     checks.assert_bit_exact(hC.numpy(), ref32, "gemm_run_host")
 
 
+@pytest.mark.parametrize("dtype,M,N,K,alpha,beta", [("tf32", 2300, 3000, 1800, 1.0, 0.0),
+                                                    ("bf16", 4096, 2048, 4096, 1.5, 0.5)])
+def test_run_host_in_row_blocks(dtype, M, N, K, alpha, beta):
+    # Large enough for gemm_run_host's row blocks (copies in, GEMMs and copies
+    # out overlapping on three streams): the oracle's bits, on two calls in a
+    # row (the second reuses the block plans), and the stream waits for it all.
+    A, B, C0 = si.problem(M, N, K, dtype, "dyadic", 16, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, alpha, beta, dtype)
+    tdt = {"tf32": torch.float32, "bf16": torch.bfloat16}[dtype]
+    hA = torch.from_numpy(A).view(tdt).pin_memory() if dtype == "bf16" else torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).view(tdt).pin_memory() if dtype == "bf16" else torch.from_numpy(B).pin_memory()
+    dA, dB = torch.empty_like(hA, device="cuda"), torch.empty_like(hB, device="cuda")
+    dC = torch.empty(M, N, device="cuda")
+    with sat.Plan(M, N, K, dtype) as plan:
+        for call in range(2):
+            hC = torch.from_numpy(C0.copy()).pin_memory()
+            sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, alpha, beta, dA, dB, dC, stream()))
+            torch.cuda.current_stream().synchronize()
+            checks.assert_bit_exact(hC.numpy(), ref32, f"gemm_run_host in row blocks, call {call + 1}")
+        sat.check(plan.status())
+
+
 def test_plan_runs_on_two_streams():
     M, N, K = 384, 512, 256
     A, B, _ = si.problem(M, N, K, "bf16", "dyadic", 14)
