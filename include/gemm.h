@@ -175,8 +175,9 @@ int gemm_run_ex(const gemm_plan* plan, const void* A, int64_t lda, const void* B
  * dC -> hC, all ordered on `cuda_stream` (after its earlier work, before its
  * later work). dA, dB, dC are caller-owned device buffers of the full
  * operand sizes. Large untransposed plans with fp32 C (M >= 1024 and at least
- * 32 MiB of A and B) run in up to 4 row blocks whose copies overlap the
- * GEMMs: the copies go on two streams of the calling stream's own (made by
+ * 32 MiB of A and B) run in up to 8 row blocks of 512 rows or more, whose
+ * copies overlap the GEMMs: the copies go on two streams of the calling
+ * stream's own (made by
  * the plan's first such run on it), the blocks' GEMMs on `cuda_stream`
  * through plans of the block's shape (made by the first such run and kept
  * with the plan; gemm_plan_status reports their bounded-wait timeouts too).

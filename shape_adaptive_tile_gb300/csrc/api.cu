@@ -99,10 +99,14 @@ struct Scratch {
     // host) and their events (start, one per block copied in, one per block
     // computed, end).
     cudaStream_t cp_in = nullptr, cp_out = nullptr;
-    cudaEvent_t hev[2 + 2 * 4] = {};
+    cudaEvent_t hev[2 + 2 * 8] = {};
 };
 constexpr int kMaxScratch = 8;
-constexpr int kHostBlocks = 4;  // row blocks of a pipelined gemm_run_host
+// Row blocks of a pipelined gemm_run_host: at most 8 (the last block's GEMM
+// and copy out are the part that overlaps nothing), of at least 512 rows.
+constexpr int kHostBlocks = 8;
+constexpr int64_t kHostMinRows = 512;
+static_assert(sizeof(Scratch::hev) / sizeof(cudaEvent_t) == 2 + 2 * kHostBlocks, "one event per block copied in and computed");
 constexpr int kTicketPad = 32;  // the ticket counter sits 128 bytes past the last CTA counter
 
 }  // namespace
@@ -929,7 +933,7 @@ int gemm_run_host(const gemm_plan* p, const void* hA, const void* hB, float* hC,
     const size_t in_bytes = static_cast<size_t>(p->M * p->K + p->K * p->N) * es;
     if (p->K > 0 && alpha != 0.0f && !p->trans_a && !p->trans_b && p->c_half == 0 && p->M >= 1024 &&
         in_bytes >= (size_t(32) << 20)) {
-        const int64_t blk = ((p->M + kHostBlocks - 1) / kHostBlocks + 255) / 256 * 256;
+        const int64_t blk = std::max(kHostMinRows, ((p->M + kHostBlocks - 1) / kHostBlocks + 255) / 256 * 256);
         const int nb = static_cast<int>((p->M + blk - 1) / blk);
         const int64_t last = p->M - (nb - 1) * blk;
         gemm_plan* sub[2] = {nullptr, nullptr};
