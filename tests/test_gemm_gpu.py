@@ -463,6 +463,30 @@ def test_run_host_in_row_blocks(dtype, M, N, K, alpha, beta):
         sat.check(plan.status())
 
 
+def test_run_host_in_row_blocks_on_two_streams():
+    # One plan, two overlapping gemm_run_host calls on two streams, each with
+    # its own buffers: each stream gets its own copy streams and scratch, the
+    # block plans are shared, and each result is the oracle's bits.
+    M, N, K = 2304, 2048, 2048   # 36 MB of A and B: 5 row blocks (4 of 512 rows, then 256)
+    probs = [si.problem(M, N, K, "tf32", "dyadic", 60 + i, "dyadic") for i in range(2)]
+    refs = [oracle.gemm(A, B, C0, 1.5, 0.5, "tf32")[1] for A, B, C0 in probs]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    bufs = []
+    for A, B, C0 in probs:
+        hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+        hC = torch.from_numpy(C0.copy()).pin_memory()
+        bufs.append((hA, hB, hC, torch.empty_like(hA, device="cuda"), torch.empty_like(hB, device="cuda"),
+                     torch.empty(M, N, device="cuda")))
+    with sat.Plan(M, N, K, "tf32") as plan:
+        for s, (hA, hB, hC, dA, dB, dC) in zip(streams, bufs):
+            sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, 1.5, 0.5, dA, dB, dC, s.cuda_stream))
+        for s in streams:
+            s.synchronize()
+        sat.check(plan.status())
+    for i, (buf, ref32) in enumerate(zip(bufs, refs)):
+        checks.assert_bit_exact(buf[2].numpy(), ref32, f"gemm_run_host on stream {i}")
+
+
 def test_plan_runs_on_two_streams():
     M, N, K = 384, 512, 256
     A, B, _ = si.problem(M, N, K, "bf16", "dyadic", 14)
