@@ -463,6 +463,23 @@ def test_run_host_in_row_blocks(dtype, M, N, K, alpha, beta):
         sat.check(plan.status())
 
 
+def test_run_host_in_row_blocks_from_pageable_memory():
+    # Host buffers that are not pinned: the copies are then synchronous for
+    # the host, and the row blocks still give the oracle's bits.
+    M, N, K = 2304, 2048, 2048
+    A, B, C0 = si.problem(M, N, K, "tf32", "dyadic", 62, "dyadic")
+    _, ref32 = oracle.gemm(A, B, C0, 1.5, 0.5, "tf32")
+    hA, hB, hC = torch.from_numpy(A), torch.from_numpy(B), torch.from_numpy(C0.copy())
+    assert not hA.is_pinned() and not hC.is_pinned()
+    dA, dB = torch.empty_like(hA, device="cuda"), torch.empty_like(hB, device="cuda")
+    dC = torch.empty(M, N, device="cuda")
+    with sat.Plan(M, N, K, "tf32") as plan:
+        sat.check(sat.gemm_run_host(plan.handle, hA, hB, hC, 1.5, 0.5, dA, dB, dC, stream()))
+        torch.cuda.current_stream().synchronize()
+        sat.check(plan.status())
+    checks.assert_bit_exact(hC.numpy(), ref32, "gemm_run_host from pageable memory")
+
+
 def test_run_host_in_row_blocks_on_two_streams():
     # One plan, two overlapping gemm_run_host calls on two streams, each with
     # its own buffers: each stream gets its own copy streams and scratch, the
